@@ -1,0 +1,166 @@
+/*
+ * lora.h — C ABI of the GB300 (sm_103a) LoRA linear layer.
+ *
+ * The layer, as the LoRAFusion write-ups state it (Eurosys26 LoRAFusion
+ * article, juhe.plus, section 2 "background"; LoRAFusion notes,
+ * papers.chlience.com, section 5 "FusedLoRA" / "FusedMultiLoRA"):
+ *
+ *     Y = X W + alpha * (dropout(X) A) B = X W + alpha * S B,   S = X_hat A
+ *
+ * with W frozen and only A, B trained.  Shapes: X m x k, W k x n, A k x r,
+ * B r x n, Y m x n.  Every matrix is row-major bf16 (its bit pattern passed
+ * as uint16_t) unless stated otherwise.  Arithmetic accumulates in fp32.
+ *
+ * Dropout (the pages fix no generator; the reading taken here): inverted
+ * dropout on the branch input, kept elements scaled by q = 1/(1-p).  The keep
+ * decision of element (t, j) — t the global row of the packed batch, j the
+ * feature — is lane j%8 of Philox4x32-10 (Salmon et al., SC'11) with key
+ * (seed low word, seed high word) and counter (t, j/8, 0, 0): the four
+ * output words give eight 16-bit lanes, low half first, and the element is
+ * kept iff lane >= T, T = floor(p*65536 + 0.5).  The backward regenerates
+ * the decisions from the seed; nothing is stored between the calls except
+ * S_saved.
+ *
+ * Multi-adapter form (LoRAFusion notes, section 5 "FusedMultiLoRA"; article
+ * section 4.1): rows are grouped in 128-row tiles; a segment table assigns
+ * each tile to one adapter (A_i, B_i, alpha_i, p_i); the frozen product X W
+ * is shared by every row, the branch of a tile uses its own adapter, and the
+ * gradients of each adapter sum over that adapter's rows only.  Rows that no
+ * segment covers get no branch (Y = X W, dX = dY W^T there).
+ *
+ * Conventions for every entry point below:
+ *  - Device pointers are device memory of the current CUDA device; the caller
+ *    owns every buffer.  The library never allocates or frees memory.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronising.  A kernel that gives
+ *    up on a bounded internal wait records a code in the workspace; read it
+ *    with lora_device_status().
+ *  - Validation happens before any launch; a failing call enqueues nothing
+ *    and returns a status.  Nothing is thrown across this interface.
+ *  - k and n must be multiples of 8, ranks multiples of 8 in [8, 128], every
+ *    pointer 16-byte aligned, 0 <= p < 1, m <= 262144 rows.
+ *  - Gradients dA, dB are overwritten, not accumulated.
+ *  - `workspace` is device memory of at least lora_workspace_size() bytes,
+ *    256-byte aligned.  One workspace must not be used by two calls that may
+ *    run concurrently.
+ */
+#ifndef LORA_GB300_H
+#define LORA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lora_bf16; /* bfloat16 bit pattern */
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_EINVAL = 1,          /* missing pointer, p outside [0,1), rank outside [8,128], ... */
+    LORA_EALIGN = 2,          /* a pointer is not 16-byte aligned (workspace: 256) */
+    LORA_ESHAPE = 3,          /* k or n not a multiple of 8, m too large, empty k or n */
+    LORA_EARCH = 4,           /* the current device is not an sm_103 GPU */
+    LORA_ECUDA = 5,           /* a CUDA runtime or driver call failed */
+    LORA_EWORKSPACE = 6,      /* workspace missing, misaligned or too small */
+    LORA_EDEVICE_TIMEOUT = 7, /* a kernel gave up on a bounded wait (from lora_device_status) */
+    LORA_ETABLE = 8           /* segment table invalid: overlap, misalignment, bad adapter id */
+} lora_status;
+
+enum { LORA_TILE_ROWS = 128, LORA_MAX_RANK = 128, LORA_MAX_ADAPTERS = 16, LORA_MAX_ROWS = 262144 };
+
+/* One adapter of the multi-adapter form.  A_i is k x rank, B_i is rank x n;
+ * dA_i / dB_i (same shapes) are written by multi_lora_bwd and may be NULL
+ * for multi_lora_fwd. */
+typedef struct {
+    int32_t rank;
+    float alpha;
+    float p;
+    const lora_bf16* A;
+    const lora_bf16* B;
+    lora_bf16* dA;
+    lora_bf16* dB;
+} lora_adapter;
+
+/* Rows [row_start, row_start + rows) use adapter `adapter`.  row_start is a
+ * multiple of 128; rows is a multiple of 128 unless the segment ends at row m.
+ * Segments must not overlap.  (Padding rows inside a segment are ordinary
+ * rows: callers that pad samples to whole tiles put zeros there.) */
+typedef struct {
+    int64_t row_start;
+    int64_t rows;
+    int32_t adapter;
+    int32_t reserved;
+} lora_segment;
+
+/* Workspace bytes sufficient for every call below with these sizes
+ * (r_max: the largest rank; n_adapters: adapters per call, >= 1). */
+size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters);
+
+/* Forward, one adapter.  Writes Y (m x n), S_saved (m x r: alpha * S in bf16,
+ * opaque state for lora_bwd) and, if mask_bits is not NULL, the keep
+ * decisions: bit j%8 of byte t*(k/8) + j/8.
+ * Steps (article section 4.1, forward ① and ②): dropout fused with the
+ * down-projection, then X W + alpha S B as one contraction [X | alpha S][W; B]. */
+lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
+                     float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r,
+                     lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward, one adapter, W frozen.  Inputs: dY (m x n), the forward's X, W,
+ * A, B, S_saved and the same alpha, p, seed.  Writes
+ *   dX = dY W^T + (D q) * (dS A^T),  dA = X_hat^T dS,  dB = alpha S^T dY,
+ * with dS = alpha dY B^T (article section 4.1, backward ③ and ⑤). */
+lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
+                     const lora_bf16* B, const lora_bf16* S_saved, float alpha, float p, uint64_t seed,
+                     int64_t m, int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Forward, packed multi-adapter batch.  `adapters` and `segments` are HOST
+ * arrays, read before the call returns.  S_saved is m x s_ld with
+ * s_ld = the largest adapter rank; row t of adapter i holds alpha_i S in
+ * columns [0, r_i) and zeros after; rows without an adapter are zero.
+ * mask_bits (optional) is written for rows that have an adapter.
+ * n_adapters may be 0 only with n_segments == 0 (the frozen layer alone). */
+lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters, int32_t n_adapters,
+                           const lora_segment* segments, int32_t n_segments, uint64_t seed, int64_t m, int64_t k,
+                           int64_t n, lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of multi_lora_fwd.  Writes dX (m x k) and every adapter's dA_i,
+ * dB_i (adapters without rows get zeros). */
+lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters,
+                           int32_t n_adapters, const lora_segment* segments, int32_t n_segments, uint64_t seed,
+                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
+/* Host only, no GPU needed: the routing table.  tile_adapter[i] (i < ceil(m/128))
+ * receives the adapter of tile i, -1 where no segment covers it. */
+lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, int32_t n_adapters, int64_t m,
+                            int32_t* tile_adapter, int64_t n_tiles);
+
+/* Host only: the keep threshold T for drop rate p (LORA_EINVAL outside [0,1)). */
+lora_status lora_keep_threshold(float p, uint32_t* T);
+
+/* Synchronises `stream`, then reads and clears the device status word of
+ * `workspace`.  *code receives the raw device code (0 = none).  Returns
+ * LORA_EDEVICE_TIMEOUT if a kernel gave up on a bounded wait. */
+lora_status lora_device_status(void* workspace, void* stream, int32_t* code);
+
+/* Sets the bound, in nanoseconds, after which a kernel stops waiting on an
+ * internal barrier, records LORA_EDEVICE_TIMEOUT and returns (default 2 s). */
+void lora_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook for the bounded waits: launches one kernel that waits on a
+ * barrier nothing will complete, with the current limit, and returns.  The
+ * device status then reads LORA_EDEVICE_TIMEOUT; the context stays usable. */
+lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void* stream);
+
+const char* lora_status_string(lora_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_GB300_H */

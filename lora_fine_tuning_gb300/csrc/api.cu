@@ -1,0 +1,564 @@
+// C ABI of the LoRA linear layer: validation, routing tables, tensor maps,
+// workspace layout and the launch sequence of each call.  See include/lora.h
+// for the contract of every entry point.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+#include "lora.h"
+#include "plan.h"
+
+namespace lora {
+namespace {
+
+// ---------------------------------------------------------------------------
+// per-device setup
+// ---------------------------------------------------------------------------
+
+struct DeviceState {
+    bool ready = false;
+    lora_status status = LORA_OK;
+    int sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+uint64_t g_wait_ns = 2000000000ull;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+lora_status device_setup(int* sms_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return LORA_ECUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        d.ready = true;
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            d.status = LORA_ECUDA;
+        } else if (major != 10 || minor != 3) {
+            d.status = LORA_EARCH;
+        } else {
+            d.sms = sms;
+            if (down_configure() != cudaSuccess || gemm_configure() != cudaSuccess ||
+                dsdb_configure() != cudaSuccess || da_configure() != cudaSuccess)
+                d.status = LORA_ECUDA;
+        }
+        if (d.status == LORA_OK && g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                d.status = LORA_ECUDA;
+            else
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    if (d.status != LORA_OK) return d.status;
+    *sms_out = d.sms;
+    return LORA_OK;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// `ld` elements between rows.
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+              uint32_t box_outer, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+CUtensorMapSwizzle rank_swizzle_host(int rpad) {
+    return rpad <= 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (rpad <= 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// ---------------------------------------------------------------------------
+// validation helpers
+// ---------------------------------------------------------------------------
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int rank_pad(int r) {
+    int p = 16;
+    while (p < r) p <<= 1;
+    return p;
+}
+
+uint32_t keep_threshold(float p) {
+    return static_cast<uint32_t>(std::floor(static_cast<double>(p) * 65536.0 + 0.5));
+}
+
+lora_status check_dims(int64_t m, int64_t k, int64_t n) {
+    if (m < 0 || k <= 0 || n <= 0) return LORA_ESHAPE;
+    if (k % 8 || n % 8) return LORA_ESHAPE;
+    if (m > LORA_MAX_ROWS) return LORA_ESHAPE;
+    if (k > (1LL << 30) || n > (1LL << 30)) return LORA_ESHAPE;
+    return LORA_OK;
+}
+
+lora_status check_adapter(const lora_adapter& a, bool need_grads) {
+    if (a.rank < 8 || a.rank > LORA_MAX_RANK || a.rank % 8) return LORA_EINVAL;
+    if (!(a.p >= 0.f && a.p < 1.f)) return LORA_EINVAL;
+    if (!std::isfinite(a.alpha)) return LORA_EINVAL;
+    if (!a.A || !a.B) return LORA_EINVAL;
+    if (!aligned16(a.A) || !aligned16(a.B)) return LORA_EALIGN;
+    if (need_grads) {
+        if (!a.dA || !a.dB) return LORA_EINVAL;
+        if (!aligned16(a.dA) || !aligned16(a.dB)) return LORA_EALIGN;
+    }
+    return LORA_OK;
+}
+
+// Segment table -> per-tile adapter (the routing table of the multi-adapter form).
+lora_status tile_table(const lora_segment* seg, int32_t nseg, int32_t nad, int64_t m, int8_t* owner, int64_t n_tiles) {
+    for (int64_t i = 0; i < n_tiles; ++i) owner[i] = -1;
+    if (nseg < 0 || (nseg > 0 && !seg)) return LORA_EINVAL;
+    for (int32_t s = 0; s < nseg; ++s) {
+        const lora_segment& g = seg[s];
+        if (g.rows == 0) continue;
+        if (g.row_start < 0 || g.rows < 0 || g.row_start + g.rows > m) return LORA_ETABLE;
+        if (g.row_start % LORA_TILE_ROWS) return LORA_ETABLE;
+        if (g.rows % LORA_TILE_ROWS && g.row_start + g.rows != m) return LORA_ETABLE;
+        if (g.adapter < 0 || g.adapter >= nad) return LORA_ETABLE;
+        const int64_t t0 = g.row_start / LORA_TILE_ROWS;
+        const int64_t t1 = (g.row_start + g.rows + LORA_TILE_ROWS - 1) / LORA_TILE_ROWS;
+        for (int64_t t = t0; t < t1; ++t) {
+            if (owner[t] != -1) return LORA_ETABLE;
+            owner[t] = static_cast<int8_t>(g.adapter);
+        }
+    }
+    return LORA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// workspace
+// ---------------------------------------------------------------------------
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+    size_t status = 0;      // int32 device status word
+    size_t s_acc = 0;       // m x s_ld fp32 (forward S, backward dS)
+    size_t dsq = 0;         // m x s_ld bf16
+    size_t acc = 0;         // per-adapter dB^T (n x rpad) and dA (k x rpad) fp32
+    size_t acc_floats = 0;
+    size_t total = 0;
+};
+
+Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int nad) {
+    Layout L;
+    size_t off = 0;
+    L.status = off;
+    off += kAlign;
+    L.s_acc = off;
+    off = up(off + static_cast<size_t>(m) * s_ld * 4);
+    L.dsq = off;
+    off = up(off + static_cast<size_t>(m) * s_ld * 2);
+    L.acc = off;
+    size_t floats = 0;
+    for (int a = 0; a < nad; ++a) floats += static_cast<size_t>(n + k) * rpads[a];
+    L.acc_floats = floats;
+    off = up(off + floats * 4);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------
+// one prepared call
+// ---------------------------------------------------------------------------
+
+struct Call {
+    Routing rt;
+    int s_ld = 0;
+    int rpads[kMaxAdapters] = {};
+    Layout L;
+    uint8_t* ws = nullptr;
+    int sms = 0;
+    cudaStream_t stream = nullptr;
+};
+
+lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_segment* seg, int32_t nseg, int64_t m,
+                    int64_t k, int64_t n, bool need_grads, void* workspace, size_t ws_bytes, void* stream) {
+    lora_status st = check_dims(m, k, n);
+    if (st) return st;
+    if (nad < 0 || nad > kMaxAdapters) return LORA_EINVAL;
+    if (nad == 0 && nseg != 0) return LORA_ETABLE;
+    if (nad > 0 && !ads) return LORA_EINVAL;
+    std::memset(&c.rt, 0, sizeof(c.rt));
+    c.rt.n_adapters = nad;
+    c.rt.rpad_max = 16;
+    int s_ld = 0;
+    for (int a = 0; a < nad; ++a) {
+        st = check_adapter(ads[a], need_grads);
+        if (st) return st;
+        AdapterDev& d = c.rt.ad[a];
+        d.rank = ads[a].rank;
+        d.rpad = rank_pad(ads[a].rank);
+        d.T = keep_threshold(ads[a].p);
+        d.scale = static_cast<float>(static_cast<double>(ads[a].alpha) / (1.0 - static_cast<double>(ads[a].p)));
+        c.rpads[a] = d.rpad;
+        c.rt.rpad_max = std::max(c.rt.rpad_max, d.rpad);
+        s_ld = std::max(s_ld, d.rank);
+    }
+    c.s_ld = s_ld;
+    const int64_t n_tiles = (m + kTileM - 1) / kTileM;
+    if (n_tiles > kMaxTiles) return LORA_ESHAPE;
+    c.rt.n_tiles = static_cast<int32_t>(n_tiles);
+    st = tile_table(seg, nseg, nad, m, c.rt.tile_adapter, n_tiles);
+    if (st) return st;
+    // group active tiles by adapter (ascending tile id within a group)
+    int count[kMaxAdapters + 1] = {};
+    for (int64_t t = 0; t < n_tiles; ++t)
+        if (c.rt.tile_adapter[t] >= 0) ++count[c.rt.tile_adapter[t]];
+    c.rt.adapter_begin[0] = 0;
+    for (int a = 0; a < kMaxAdapters; ++a) c.rt.adapter_begin[a + 1] = c.rt.adapter_begin[a] + (a < nad ? count[a] : 0);
+    int fill[kMaxAdapters] = {};
+    for (int64_t t = 0; t < n_tiles; ++t) {
+        const int a = c.rt.tile_adapter[t];
+        if (a >= 0) c.rt.active_tiles[c.rt.adapter_begin[a] + fill[a]++] = static_cast<uint16_t>(t);
+    }
+    c.rt.n_active = c.rt.adapter_begin[nad > 0 ? nad : 0];
+    // workspace
+    c.L = layout(m, k, n, s_ld, c.rpads, nad);
+    int64_t off = 0;
+    for (int a = 0; a < nad; ++a) {
+        c.rt.ad[a].dB_off = off;
+        off += n * c.rpads[a];
+        c.rt.ad[a].dA_off = off;
+        off += k * c.rpads[a];
+    }
+    if (!workspace) return LORA_EWORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LORA_EWORKSPACE;
+    if (ws_bytes < c.L.total) return LORA_EWORKSPACE;
+    c.ws = static_cast<uint8_t*>(workspace);
+    st = device_setup(&c.sms);
+    if (st) return st;
+    c.stream = static_cast<cudaStream_t>(stream);
+    return LORA_OK;
+}
+
+DevCtl ctl_of(const Call& c) { return DevCtl{reinterpret_cast<int*>(c.ws + c.L.status), g_wait_ns}; }
+
+#define LORA_CUDA(expr)                                  \
+    do {                                                 \
+        if ((expr) != cudaSuccess) return LORA_ECUDA;    \
+    } while (0)
+
+lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const lora_adapter* ads, uint64_t seed,
+                    int64_t m, int64_t k, int64_t n, uint16_t* Y, uint16_t* S_saved, uint8_t* mask_bits) {
+    if (m == 0) return LORA_OK;
+    const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
+    const int nad = c.rt.n_adapters;
+    float* s_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
+
+    if (nad > 0) {
+        LORA_CUDA(cudaMemsetAsync(s_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream));
+        if (c.rt.n_active > 0) {
+            static DownParams p;  // large: keep it off the stack
+            std::memset(&p, 0, sizeof(p));
+            if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            for (int a = 0; a < nad; ++a) {
+                const int rp = c.rpads[a];
+                if (!make_map(&p.mapA[a], ads[a].A, ads[a].rank, k, ads[a].rank, std::min(rp, 64), 64,
+                              rank_swizzle_host(rp)))
+                    return LORA_ECUDA;
+            }
+            p.rt = c.rt;
+            p.ctl = ctl_of(c);
+            p.S_acc = s_acc;
+            p.mask_bits = mask_bits;
+            p.m = m;
+            p.k = k;
+            p.ld = c.s_ld;
+            p.nkb = static_cast<int32_t>((k + 63) / 64);
+            p.units = static_cast<int64_t>(c.rt.n_active) * p.nkb;
+            p.seed_lo = seed_lo;
+            p.seed_hi = seed_hi;
+            p.stages = kDownStages;
+            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+            LORA_CUDA(launch_down(p, grid, c.stream));
+        }
+        LORA_CUDA(launch_finalize_s(s_acc, S_saved, m, c.s_ld, c.rt, c.sms, c.stream));
+    }
+
+    static GemmParams g;
+    std::memset(&g, 0, sizeof(g));
+    if (!make_map(&g.mapA, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+    if (!make_map(&g.mapB, W, n, k, n, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+    if (nad > 0) {
+        if (!make_map(&g.mapTA, S_saved, c.s_ld, m, c.s_ld, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        for (int a = 0; a < nad; ++a)
+            if (!make_map(&g.mapTB[a], ads[a].B, n, ads[a].rank, n, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+                return LORA_ECUDA;
+    }
+    g.rt = c.rt;
+    g.ctl = ctl_of(c);
+    g.out = Y;
+    g.M = m;
+    g.N = n;
+    g.K = k;
+    g.n_mtiles = static_cast<int32_t>((m + 127) / 128);
+    g.n_ntiles = static_cast<int32_t>((n + 255) / 256);
+    g.nkb = static_cast<int32_t>((k + 63) / 64);
+    g.group_m = 16;
+    g.seed_lo = seed_lo;
+    g.seed_hi = seed_hi;
+    const int tiles = g.n_mtiles * g.n_ntiles;
+    LORA_CUDA(launch_gemm_fwd(g, std::min(tiles, c.sms), c.stream));
+    return LORA_OK;
+}
+
+lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const uint16_t* W, const lora_adapter* ads,
+                    uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, uint16_t* dX) {
+    const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
+    const int nad = c.rt.n_adapters;
+    float* ds_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
+    uint16_t* dsq = reinterpret_cast<uint16_t*>(c.ws + c.L.dsq);
+    float* acc = reinterpret_cast<float*>(c.ws + c.L.acc);
+    AdapterPtrs dBp{}, dAp{};
+    for (int a = 0; a < nad; ++a) {
+        dBp.p[a] = ads[a].dB;
+        dAp.p[a] = ads[a].dA;
+    }
+
+    if (nad > 0) {
+        if (m > 0) LORA_CUDA(cudaMemsetAsync(ds_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream));
+        LORA_CUDA(cudaMemsetAsync(acc, 0, c.L.acc_floats * 4, c.stream));
+        if (c.rt.n_active > 0) {
+            static DsDbParams p;
+            std::memset(&p, 0, sizeof(p));
+            if (!make_map(&p.mapDY, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            for (int a = 0; a < nad; ++a) {
+                const int rp = c.rpads[a];
+                if (!make_map(&p.mapB[a], ads[a].B, n, ads[a].rank, n, 64, rp, CU_TENSOR_MAP_SWIZZLE_128B))
+                    return LORA_ECUDA;
+                if (!make_map(&p.mapS[a], S_saved, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
+                    return LORA_ECUDA;
+            }
+            p.rt = c.rt;
+            p.ctl = ctl_of(c);
+            p.dS_acc = ds_acc;
+            p.acc_base = acc;
+            p.m = m;
+            p.n = n;
+            p.ld = c.s_ld;
+            p.nnb = static_cast<int32_t>((n + 127) / 128);
+            p.units = static_cast<int64_t>(c.rt.n_active) * p.nnb;
+            const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
+            p.off_b = 32768;
+            p.off_s = p.off_b + 2 * 128 * rpm;
+            p.stage_bytes = p.off_s + 256 * rpm;
+            p.stages = static_cast<int32_t>(std::min<size_t>(8, (220 * 1024) / p.stage_bytes));
+            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+            LORA_CUDA(launch_dsdb(p, grid, c.stream));
+        }
+        LORA_CUDA(launch_finalize_bwd1(ds_acc, dsq, m, c.s_ld, acc, dBp, n, c.rt, c.sms, c.stream));
+    }
+
+    if (m > 0) {
+        static GemmParams g;
+        std::memset(&g, 0, sizeof(g));
+        if (!make_map(&g.mapA, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        if (!make_map(&g.mapB, W, n, k, n, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        if (nad > 0) {
+            if (!make_map(&g.mapTA, dsq, c.s_ld, m, c.s_ld, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            for (int a = 0; a < nad; ++a)
+                if (!make_map(&g.mapTB[a], ads[a].A, ads[a].rank, k, ads[a].rank, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+                    return LORA_ECUDA;
+        }
+        g.rt = c.rt;
+        g.ctl = ctl_of(c);
+        g.out = dX;
+        g.M = m;
+        g.N = k;
+        g.K = n;
+        g.n_mtiles = static_cast<int32_t>((m + 127) / 128);
+        g.n_ntiles = static_cast<int32_t>((k + 255) / 256);
+        g.nkb = static_cast<int32_t>((n + 63) / 64);
+        g.group_m = 16;
+        g.seed_lo = seed_lo;
+        g.seed_hi = seed_hi;
+        const int tiles = g.n_mtiles * g.n_ntiles;
+        LORA_CUDA(launch_gemm_bwd(g, std::min(tiles, c.sms), c.stream));
+    }
+
+    if (nad > 0) {
+        if (c.rt.n_active > 0) {
+            static DaParams p;
+            std::memset(&p, 0, sizeof(p));
+            if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+            for (int a = 0; a < nad; ++a) {
+                const int rp = c.rpads[a];
+                if (!make_map(&p.mapD[a], dsq, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
+                    return LORA_ECUDA;
+            }
+            p.rt = c.rt;
+            p.ctl = ctl_of(c);
+            p.acc_base = acc;
+            p.m = m;
+            p.k = k;
+            p.nfb = static_cast<int32_t>((k + 127) / 128);
+            int64_t u = 0;
+            for (int a = 0; a <= nad; ++a) {
+                p.unit_begin[a] = u;
+                if (a < nad) u += static_cast<int64_t>(p.nfb) * (c.rt.adapter_begin[a + 1] - c.rt.adapter_begin[a]);
+            }
+            for (int a = nad + 1; a <= kMaxAdapters; ++a) p.unit_begin[a] = u;
+            p.units = u;
+            p.seed_lo = seed_lo;
+            p.seed_hi = seed_hi;
+            const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
+            p.off_d = 32768;
+            p.stage_bytes = p.off_d + 256 * rpm;
+            p.stages = static_cast<int32_t>(std::min<size_t>(8, (220 * 1024) / p.stage_bytes));
+            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+            LORA_CUDA(launch_da(p, grid, c.stream));
+        }
+        LORA_CUDA(launch_finalize_da(acc, dAp, k, c.rt, c.sms, c.stream));
+    }
+    return LORA_OK;
+}
+
+std::mutex g_call_mu;  // the static parameter blocks above are shared
+
+}  // namespace
+}  // namespace lora
+
+using namespace lora;
+
+extern "C" {
+
+size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters) {
+    if (m < 0 || k < 0 || n < 0 || r_max < 0 || n_adapters < 0) return 0;
+    int rp[kMaxAdapters];
+    const int nad = std::min<int32_t>(std::max<int32_t>(n_adapters, 1), kMaxAdapters);
+    for (int a = 0; a < nad; ++a) rp[a] = rank_pad(std::max(r_max, 8));
+    return layout(m, k, n, std::max(r_max, 8), rp, nad).total;
+}
+
+lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters, int32_t n_adapters,
+                           const lora_segment* segments, int32_t n_segments, uint64_t seed, int64_t m, int64_t k,
+                           int64_t n, lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (!W || (m > 0 && (!X || !Y))) return LORA_EINVAL;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved)) return LORA_EALIGN;
+    if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
+    std::lock_guard<std::mutex> lock(g_call_mu);
+    static Call c;
+    lora_status st = prepare(c, adapters, n_adapters, segments, n_segments, m, k, n, false, workspace,
+                             workspace_bytes, stream);
+    if (st) return st;
+    return run_fwd(c, X, W, adapters, seed, m, k, n, Y, S_saved, mask_bits);
+}
+
+lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters,
+                           int32_t n_adapters, const lora_segment* segments, int32_t n_segments, uint64_t seed,
+                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    if (!W || (m > 0 && (!X || !dY || !dX))) return LORA_EINVAL;
+    if (!aligned16(dY) || !aligned16(X) || !aligned16(W) || !aligned16(dX) || !aligned16(S_saved))
+        return LORA_EALIGN;
+    if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
+    std::lock_guard<std::mutex> lock(g_call_mu);
+    static Call c;
+    lora_status st = prepare(c, adapters, n_adapters, segments, n_segments, m, k, n, true, workspace,
+                             workspace_bytes, stream);
+    if (st) return st;
+    return run_bwd(c, dY, X, W, adapters, seed, m, k, n, S_saved, dX);
+}
+
+lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B, float alpha,
+                     float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r, lora_bf16* Y,
+                     lora_bf16* S_saved, uint8_t* mask_bits, void* workspace, size_t workspace_bytes, void* stream) {
+    lora_adapter ad{r, alpha, p, A, B, nullptr, nullptr};
+    lora_segment seg{0, m, 0, 0};
+    return multi_lora_fwd(X, W, &ad, 1, &seg, m > 0 ? 1 : 0, seed, m, k, n, Y, S_saved, mask_bits, workspace,
+                          workspace_bytes, stream);
+}
+
+lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
+                     const lora_bf16* B, const lora_bf16* S_saved, float alpha, float p, uint64_t seed, int64_t m,
+                     int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    lora_adapter ad{r, alpha, p, A, B, dA, dB};
+    lora_segment seg{0, m, 0, 0};
+    return multi_lora_bwd(dY, X, W, &ad, 1, &seg, m > 0 ? 1 : 0, seed, m, k, n, S_saved, dX, workspace,
+                          workspace_bytes, stream);
+}
+
+lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, int32_t n_adapters, int64_t m,
+                            int32_t* tile_adapter, int64_t n_tiles) {
+    if (m < 0 || m > LORA_MAX_ROWS || n_adapters < 0 || n_adapters > kMaxAdapters) return LORA_EINVAL;
+    const int64_t need = (m + kTileM - 1) / kTileM;
+    if (!tile_adapter || n_tiles < need) return LORA_EINVAL;
+    static int8_t owner[kMaxTiles];
+    std::lock_guard<std::mutex> lock(g_call_mu);
+    lora_status st = tile_table(segments, n_segments, n_adapters, m, owner, need);
+    if (st) return st;
+    for (int64_t t = 0; t < need; ++t) tile_adapter[t] = owner[t];
+    return LORA_OK;
+}
+
+lora_status lora_keep_threshold(float p, uint32_t* T) {
+    if (!T || !(p >= 0.f && p < 1.f)) return LORA_EINVAL;
+    *T = keep_threshold(p);
+    return LORA_OK;
+}
+
+lora_status lora_device_status(void* workspace, void* stream, int32_t* code) {
+    if (!workspace || !code) return LORA_EINVAL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return LORA_ECUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ECUDA;
+    if (v != 0) {
+        const int32_t zero = 0;
+        if (cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return LORA_ECUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ECUDA;
+    }
+    *code = v;
+    return v != 0 ? LORA_EDEVICE_TIMEOUT : LORA_OK;
+}
+
+void lora_set_wait_limit_ns(uint64_t ns) { g_wait_ns = ns > 0 ? ns : 1; }
+
+lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace || workspace_bytes < kAlign || reinterpret_cast<uintptr_t>(workspace) % kAlign)
+        return LORA_EWORKSPACE;
+    int sms = 0;
+    lora_status st = device_setup(&sms);
+    if (st) return st;
+    DevCtl ctl{static_cast<int*>(workspace), g_wait_ns};
+    if (launch_stuck_wait(ctl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return LORA_ECUDA;
+    return LORA_OK;
+}
+
+const char* lora_status_string(lora_status s) {
+    switch (s) {
+        case LORA_OK: return "ok";
+        case LORA_EINVAL: return "invalid argument";
+        case LORA_EALIGN: return "pointer not 16-byte aligned";
+        case LORA_ESHAPE: return "unsupported shape";
+        case LORA_EARCH: return "device is not sm_103";
+        case LORA_ECUDA: return "CUDA call failed";
+        case LORA_EWORKSPACE: return "workspace missing, misaligned or too small";
+        case LORA_EDEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+        case LORA_ETABLE: return "invalid segment table";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

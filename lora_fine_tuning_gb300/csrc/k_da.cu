@@ -1,0 +1,280 @@
+// dA_a = X_hat^T dS for each adapter, with the keep mask regenerated from the seed.
+//
+// The article (juhe.plus) section 4.1 numbers the backward kernels ③ and ⑤;
+// the gradient of A is the one the list leaves out, and the definition gives
+// it: dA = X_hat^T dS = (X .* D)^T (q dS) = (X .* D)^T dSq.
+// Each unit is (adapter a, 128-feature block, one of a's 128-row tiles): two
+// TMA boxes of X (128 tokens x 64 features, 128B swizzle) plus the tile's dSq
+// rows.  Warps 2..5 zero the dropped X elements in shared memory (Philox,
+// exactly as the forward), warp 1 issues tcgen05.mma with both operands
+// MN-major (M = 128 features, N = rank, K = 128 tokens) accumulating over a
+// CTA's run of tiles of one (adapter, feature block), and the run's partial is
+// added into the adapter's fp32 accumulator with vector reductions.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kXBytes = 2u * 128u * 128u;   // 128 tokens x 128 features
+
+struct DaUnit {
+    int a, fb, ti, tile, n_a;
+};
+
+__device__ __forceinline__ DaUnit da_unit(int64_t u, const DaParams& p) {
+    int a = 0;
+    while (a + 1 < p.rt.n_adapters && p.unit_begin[a + 1] <= u) ++a;
+    const int n_a = p.rt.adapter_begin[a + 1] - p.rt.adapter_begin[a];
+    const int64_t r = u - p.unit_begin[a];
+    DaUnit d;
+    d.a = a;
+    d.n_a = n_a;
+    d.fb = static_cast<int>(r / n_a);
+    d.ti = static_cast<int>(r % n_a);
+    d.tile = p.rt.active_tiles[p.rt.adapter_begin[a] + d.ti];
+    return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__ DaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* masked = bars + S;
+    uint64_t* empty = bars + 2 * S;
+    uint64_t* acc_full = bars + 3 * S;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rpad_max = p.rt.rpad_max;
+    const uint32_t tmem_cols = static_cast<uint32_t>(2 * rpad_max) < 32u ? 32u : static_cast<uint32_t>(2 * rpad_max);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&masked[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDa << 8};
+
+    const int64_t U = p.units;
+    const int64_t u0 = U * blockIdx.x / gridDim.x;
+    const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = u0; u < u1; ++u) {
+                const DaUnit d = da_unit(u, p);
+                const int rpad = p.rt.ad[d.a].rpad;
+                if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                uint8_t* st = smem + s * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], kXBytes + 256u * static_cast<uint32_t>(rpad));
+                tma_load_2d(st, &p.mapX, &full[s], d.fb * 128, d.tile * kTileM);
+                tma_load_2d(st + 16384, &p.mapX, &full[s], d.fb * 128 + 64, d.tile * kTileM);
+                tma_load_2d(st + p.off_d, &p.mapD[d.a], &full[s], 0, d.tile * kTileM);
+                if (rpad > 64) tma_load_2d(st + p.off_d + 16384, &p.mapD[d.a], &full[s], 64, d.tile * kTileM);
+                ++issued;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t use = 0;
+            for (int64_t u = u0; u < u1; ++u) {
+                const DaUnit d = da_unit(u, p);
+                const int rpad = p.rt.ad[d.a].rpad;
+                const bool first = (u == u0) || d.ti == 0;
+                const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
+                const uint32_t b = use & 1u;
+                if (first) {
+                    if (!mbar_wait(&acc_empty[b], ((use >> 1) & 1u) ^ 1u, w, 2)) break;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&masked[s], ph, w, 3)) break;
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
+                const uint32_t idesc = make_idesc_bf16(128, rpad, true, true);
+                const uint32_t sw = rank_swizzle(rpad);
+                const uint32_t rb = rank_row_bytes(rpad);
+                const uint32_t dacc = tmem + b * static_cast<uint32_t>(rpad_max);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = make_smem_desc(st + ks * 2048u, 16384, 1024, kSw128);
+                    const uint64_t bd = make_smem_desc(st + p.off_d + ks * 16u * rb, 16384, 8u * rb, sw);
+                    umma_bf16(dacc, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
+                }
+                umma_commit(&empty[s]);
+                if (last) {
+                    umma_commit(&acc_full[b]);
+                    ++use;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else {
+        const int et = threadIdx.x - 64;
+        const int quad = warp & 3;
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t use = 0;
+        for (int64_t u = u0; u < u1; ++u) {
+            const DaUnit d = da_unit(u, p);
+            const AdapterDev ad = p.rt.ad[d.a];
+            const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
+            bool ok = mbar_wait(&full[s], ph, w, 4);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (ad.T != 0u) {
+                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
+#pragma unroll 2
+                for (int i = 0; i < 16; ++i) {
+                    const int h = i >> 3;
+                    const int ch = et + 128 * (i & 7);
+                    const int row = ch >> 3;
+                    const int c16 = ch & 7;
+                    const uint32_t addr = st + h * 16384 + row * 128 + ((c16 ^ (row & 7)) << 4);
+                    const int64_t t = static_cast<int64_t>(d.tile) * kTileM + row;
+                    const int64_t j0 = static_cast<int64_t>(d.fb) * 128 + h * 64 + c16 * 8;
+                    const uint4 wv = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(j0 >> 3), p.seed_lo,
+                                               p.seed_hi);
+                    uint4 v = lds128(addr);
+                    v.x &= keep_pair_mask(wv.x, ad.T);
+                    v.y &= keep_pair_mask(wv.y, ad.T);
+                    v.z &= keep_pair_mask(wv.z, ad.T);
+                    v.w &= keep_pair_mask(wv.w, ad.T);
+                    sts128(addr, v);
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&masked[s]);
+            if (last) {
+                const uint32_t b = use & 1u;
+                ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                const int64_t j = static_cast<int64_t>(d.fb) * 128 + quad * 32 + lane;
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * static_cast<uint32_t>(rpad_max);
+                float* dst = p.acc_base + ad.dA_off + j * ad.rpad;
+                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (j < p.k) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[b]);
+                ++use;
+            }
+            if (++s == S) { s = 0; ph ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// dA_a[j, c] = bf16(acc_a[j, c]) for c < r_a.
+__global__ void finalize_da_kernel(const float* __restrict__ acc_base, int64_t k, const __grid_constant__ Routing rt,
+                                   const __grid_constant__ AdapterPtrs dap) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    for (int a = 0; a < rt.n_adapters; ++a) {
+        const AdapterDev ad = rt.ad[a];
+        const int64_t total = k * ad.rank;
+        const float* src = acc_base + ad.dA_off;
+        uint16_t* dst = dap.p[a];
+        for (int64_t i = tid; i < total; i += stride) {
+            const int64_t j = i / ad.rank;
+            const int64_t c = i - j * ad.rank;
+            dst[i] = static_cast<uint16_t>(pack_bf16x2(src[j * ad.rpad + c], 0.f) & 0xFFFFu);
+        }
+    }
+}
+
+__global__ void stuck_wait_kernel(DevCtl ctl) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const WaitCtx w{&abort_flag, ctl.status, ctl.wait_ns, kKDebug << 8};
+    // No thread ever arrives on `bar`: the wait can only end by running out of time.
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, w, 1);
+    __syncthreads();
+}
+
+}  // namespace
+
+size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 5) * 8 + 16; }
+
+cudaError_t da_configure() {
+    return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream) {
+    da_kernel<<<grid, kThreads, da_smem_bytes(p), stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_da(const float* acc_base, const AdapterPtrs& dA, int64_t k, const Routing& rt, int sms,
+                               cudaStream_t stream) {
+    finalize_da_kernel<<<4 * sms, 256, 0, stream>>>(acc_base, k, rt, dA);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream) {
+    stuck_wait_kernel<<<1, 32, 0, stream>>>(ctl);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

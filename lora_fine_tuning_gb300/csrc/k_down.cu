@@ -1,0 +1,265 @@
+// Down-projection with fused dropout: S_acc += (X .* D) A_a, per 128-row tile.
+//
+// LoRAFusion notes (papers.chlience.com), section 5 "FusedLoRA": dropout and
+// the down-projection are one pass so the full-size X is read once; the
+// article (juhe.plus) section 4.1 lists it as forward step ①.  Here:
+//  - warp 0 streams X tiles (128 x 64, TMA, 128B swizzle) and the matching
+//    64-row block of A_a into a ring of shared-memory stages;
+//  - warps 2..5 regenerate the keep mask with Philox4x32-10 and zero the
+//    dropped elements in place (16 bytes = 8 features = one Philox call per
+//    access), then hand the stage to the MMA warp;
+//  - warp 1 issues tcgen05.mma (M = 128 tokens, N = rank, K = 64 per stage)
+//    into a double-buffered TMEM accumulator;
+//  - at the end of each tile range, warps 2..5 read TMEM and add the fp32
+//    partial into S_acc with vector reductions (ranges of one tile may be
+//    split over CTAs: units are spread evenly, stream-K style).
+// The scale alpha/(1-p) and the bf16 rounding are applied by finalize_s.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16
+constexpr uint32_t kABytes = 16384u;        // up to 64 rows x 128 bf16
+constexpr uint32_t kStageBytes = kXBytes + kABytes;
+
+__global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_constant__ DownParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    uint64_t* full = bars;
+    uint64_t* masked = bars + S;
+    uint64_t* empty = bars + 2 * S;
+    uint64_t* acc_full = bars + 3 * S;
+    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rpad_max = p.rt.rpad_max;
+    const uint32_t tmem_cols = static_cast<uint32_t>(2 * rpad_max) < 32u ? 32u : static_cast<uint32_t>(2 * rpad_max);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&masked[s], 128);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 128);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapX);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDown << 8};
+
+    const int64_t U = p.units;
+    const int64_t u0 = U * blockIdx.x / gridDim.x;
+    const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int slot = static_cast<int>(u / p.nkb);
+                const int kb = static_cast<int>(u % p.nkb);
+                const int tile = p.rt.active_tiles[slot];
+                const int a = p.rt.tile_adapter[tile];
+                const int rpad = p.rt.ad[a].rpad;
+                if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                uint8_t* xs = smem + s * kStageBytes;
+                mbar_arrive_expect_tx(&full[s], kXBytes + 128u * static_cast<uint32_t>(rpad));
+                tma_load_2d(xs, &p.mapX, &full[s], kb * 64, tile * kTileM);
+                tma_load_2d(xs + kXBytes, &p.mapA[a], &full[s], 0, kb * 64);
+                if (rpad > 64) tma_load_2d(xs + kXBytes + 8192, &p.mapA[a], &full[s], 64, kb * 64);
+                ++issued;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                // Let every copy still in flight land before the CTA can exit.
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t use = 0;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int slot = static_cast<int>(u / p.nkb);
+                const int kb = static_cast<int>(u % p.nkb);
+                const int tile = p.rt.active_tiles[slot];
+                const int a = p.rt.tile_adapter[tile];
+                const int rpad = p.rt.ad[a].rpad;
+                const bool first = (u == u0) || kb == 0;
+                const bool last = (u == u1 - 1) || kb == p.nkb - 1;
+                const uint32_t b = use & 1u;
+                if (first) {
+                    if (!mbar_wait(&acc_empty[b], ((use >> 1) & 1u) ^ 1u, w, 2)) break;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&masked[s], ph, w, 3)) break;
+                tc_fence_after();
+                const uint32_t xs = smem_u32(smem + s * kStageBytes);
+                const uint32_t as = xs + kXBytes;
+                const uint32_t idesc = make_idesc_bf16(128, rpad, false, true);
+                const uint32_t sw = rank_swizzle(rpad);
+                const uint32_t rb = rank_row_bytes(rpad);
+                const uint32_t d = tmem + b * static_cast<uint32_t>(rpad_max);
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t ad = make_smem_desc(xs + ks * 32, 16, 1024, kSw128);
+                    const uint64_t bd = make_smem_desc(as + ks * 16 * rb, 8192, 8 * rb, sw);
+                    umma_bf16(d, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
+                }
+                umma_commit(&empty[s]);
+                if (last) {
+                    umma_commit(&acc_full[b]);
+                    ++use;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            // Everything issued must complete before TMEM is released.
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else {
+        // warps 2..5: mask + epilogue.  TMEM lane quadrant = warp % 4.
+        const int et = threadIdx.x - 64;
+        const int quad = warp & 3;
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t use = 0;
+        for (int64_t u = u0; u < u1; ++u) {
+            const int slot = static_cast<int>(u / p.nkb);
+            const int kb = static_cast<int>(u % p.nkb);
+            const int tile = p.rt.active_tiles[slot];
+            const int a = p.rt.tile_adapter[tile];
+            const uint32_t T = p.rt.ad[a].T;
+            const bool last = (u == u1 - 1) || kb == p.nkb - 1;
+            bool ok = mbar_wait(&full[s], ph, w, 4);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            if (T != 0u || p.mask_bits != nullptr) {
+                const uint32_t xs = smem_u32(smem + s * kStageBytes);
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {
+                    const int ch = et + 128 * i;
+                    const int row = ch >> 3;
+                    const int c16 = ch & 7;
+                    const uint32_t addr = xs + row * 128 + ((c16 ^ (row & 7)) << 4);
+                    const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
+                    const int64_t j0 = static_cast<int64_t>(kb) * 64 + c16 * 8;
+                    const uint4 wv = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(j0 >> 3), p.seed_lo,
+                                               p.seed_hi);
+                    if (T != 0u) {
+                        uint4 v = lds128(addr);
+                        v.x &= keep_pair_mask(wv.x, T);
+                        v.y &= keep_pair_mask(wv.y, T);
+                        v.z &= keep_pair_mask(wv.z, T);
+                        v.w &= keep_pair_mask(wv.w, T);
+                        sts128(addr, v);
+                    }
+                    if (p.mask_bits != nullptr && t < p.m && j0 < p.k)
+                        p.mask_bits[t * (p.k >> 3) + (j0 >> 3)] = static_cast<uint8_t>(keep_byte(wv, T));
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&masked[s]);
+            if (last) {
+                const uint32_t b = use & 1u;
+                ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                const AdapterDev ad = p.rt.ad[a];
+                const int64_t row = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * static_cast<uint32_t>(rpad_max);
+                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (row < p.m) {
+                        float* dst = p.S_acc + row * p.ld + c0;
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&acc_empty[b]);
+                ++use;
+            }
+            if (++s == S) { s = 0; ph ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+__global__ void finalize_s_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
+                                  const __grid_constant__ Routing rt) {
+    const int64_t total = m * ld;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / ld;
+        const int c = static_cast<int>(i - t * ld);
+        const int a = rt.tile_adapter[t >> 7];
+        float v = 0.f;
+        if (a >= 0 && c < rt.ad[a].rank) v = acc[i] * rt.ad[a].scale;
+        out[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+    }
+}
+
+}  // namespace
+
+size_t down_smem_bytes(int stages) { return 1024 + stages * kStageBytes + (3 * stages + 5) * 8 + 16; }
+
+cudaError_t down_configure() {
+    return cudaFuncSetAttribute(down_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(down_smem_bytes(kDownStages)));
+}
+
+cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
+    down_proj_kernel<<<grid, kThreads, down_smem_bytes(p.stages), stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_s(const float* acc, uint16_t* out, int64_t m, int32_t ld, const Routing& rt, int sms,
+                              cudaStream_t stream) {
+    const int64_t total = m * ld;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > 4L * sms) blocks = 4L * sms;
+    if (blocks < 1) blocks = 1;
+    finalize_s_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(acc, out, m, ld, rt);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,279 @@
+// dS and dB from one read of dY.
+//
+// LoRAFusion notes (papers.chlience.com), section 5 "FusedLoRA", and the
+// article (juhe.plus) section 4.1, backward ③: the dS and dB computations are
+// fused so the full-size dY is loaded once:
+//     dS  = alpha dY B_a^T      (m x r; scaled by 1/(1-p) later: dSq)
+//     dB  = S'^T dY             (r x n; S' = alpha S from the forward)
+// Each unit is one (128-row tile, 128-wide n block) of dY, staged by TMA as two
+// 128B-swizzled 128 x 64 boxes.  The same shared-memory tile is read twice by
+// the tensor cores: K-major for dS (K = n) and MN-major for dB^T (M = n,
+// K = tokens).  dS accumulates in TMEM over a CTA's run of n blocks of one
+// tile; dB^T is produced per unit in a double-buffered accumulator.  Both are
+// flushed with fp32 vector reductions into workspace accumulators (several
+// CTAs share a tile or an n block); finalize_bwd1 scales and rounds them.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kDyBytes = 2u * 128u * 128u;   // 128 tokens x 128 n
+
+__global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant__ DsDbParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* accS_full = bars + 2 * S;
+    uint64_t* accS_empty = accS_full + 1;
+    uint64_t* accB_full = accS_empty + 1;   // [2]
+    uint64_t* accB_empty = accB_full + 2;   // [2]
+    uint64_t* drain = accB_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rpad_max = p.rt.rpad_max;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(3 * rpad_max)) tmem_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accS_full, 1);
+        mbar_init(accS_empty, 128);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accB_full[b], 1);
+            mbar_init(&accB_empty[b], 128);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapDY);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem;
+    const uint32_t tB = tmem + static_cast<uint32_t>(rpad_max);
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDsDb << 8};
+
+    const int64_t U = p.units;
+    const int64_t u0 = U * blockIdx.x / gridDim.x;
+    const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+    const uint32_t bbox = static_cast<uint32_t>(rpad_max) * 128u;   // spacing of the two B boxes
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int slot = static_cast<int>(u / p.nnb);
+                const int nb = static_cast<int>(u % p.nnb);
+                const int tile = p.rt.active_tiles[slot];
+                const int a = p.rt.tile_adapter[tile];
+                const int rpad = p.rt.ad[a].rpad;
+                if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                uint8_t* st = smem + s * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], kDyBytes + 2u * 128u * rpad + 256u * rpad);
+                tma_load_2d(st, &p.mapDY, &full[s], nb * 128, tile * kTileM);
+                tma_load_2d(st + 16384, &p.mapDY, &full[s], nb * 128 + 64, tile * kTileM);
+                tma_load_2d(st + p.off_b, &p.mapB[a], &full[s], nb * 128, 0);
+                tma_load_2d(st + p.off_b + bbox, &p.mapB[a], &full[s], nb * 128 + 64, 0);
+                tma_load_2d(st + p.off_s, &p.mapS[a], &full[s], 0, tile * kTileM);
+                if (rpad > 64) tma_load_2d(st + p.off_s + 16384, &p.mapS[a], &full[s], 64, tile * kTileM);
+                ++issued;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t units_done = 0, items_done = 0;
+            for (int64_t u = u0; u < u1; ++u) {
+                const int slot = static_cast<int>(u / p.nnb);
+                const int nb = static_cast<int>(u % p.nnb);
+                const int tile = p.rt.active_tiles[slot];
+                const int a = p.rt.tile_adapter[tile];
+                const int rpad = p.rt.ad[a].rpad;
+                const bool first = (u == u0) || nb == 0;
+                const bool last = (u == u1 - 1) || nb == p.nnb - 1;
+                if (first) {
+                    if (!mbar_wait(accS_empty, (items_done & 1u) ^ 1u, w, 2)) break;
+                    tc_fence_after();
+                }
+                const uint32_t bb = units_done & 1u;
+                if (!mbar_wait(&accB_empty[bb], ((units_done >> 1) & 1u) ^ 1u, w, 3)) break;
+                tc_fence_after();
+                if (!mbar_wait(&full[s], ph, w, 4)) break;
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
+                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad)
+                const uint32_t idesc_s = make_idesc_bf16(128, rpad, false, false);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t h = static_cast<uint32_t>(ks >> 2), kk = static_cast<uint32_t>(ks & 3);
+                    const uint64_t ad = make_smem_desc(st + h * 16384u + kk * 32u, 16, 1024, kSw128);
+                    const uint64_t bd = make_smem_desc(st + p.off_b + h * bbox + kk * 32u, 16, 1024, kSw128);
+                    umma_bf16(tS, ad, bd, idesc_s, (first && ks == 0) ? 0u : 1u);
+                }
+                // dB^T = dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens, N = rpad)
+                const uint32_t idesc_b = make_idesc_bf16(128, rpad, true, true);
+                const uint32_t sw = rank_swizzle(rpad);
+                const uint32_t rb = rank_row_bytes(rpad);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t ad = make_smem_desc(st + ks * 2048u, 16384, 1024, kSw128);
+                    const uint64_t bd = make_smem_desc(st + p.off_s + ks * 16u * rb, 16384, 8u * rb, sw);
+                    umma_bf16(tB + bb * static_cast<uint32_t>(rpad_max), ad, bd, idesc_b, ks != 0 ? 1u : 0u);
+                }
+                umma_commit(&empty[s]);
+                umma_commit(&accB_full[bb]);
+                ++units_done;
+                if (last) {
+                    umma_commit(accS_full);
+                    ++items_done;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else {
+        const int quad = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t units_done = 0, items_done = 0;
+        for (int64_t u = u0; u < u1; ++u) {
+            const int slot = static_cast<int>(u / p.nnb);
+            const int nb = static_cast<int>(u % p.nnb);
+            const int tile = p.rt.active_tiles[slot];
+            const int a = p.rt.tile_adapter[tile];
+            const AdapterDev ad = p.rt.ad[a];
+            const bool last = (u == u1 - 1) || nb == p.nnb - 1;
+            const uint32_t bb = units_done & 1u;
+            bool ok = mbar_wait(&accB_full[bb], (units_done >> 1) & 1u, w, 5);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            {
+                const int64_t nidx = static_cast<int64_t>(nb) * 128 + quad * 32 + lane;
+                float* dst = p.acc_base + ad.dB_off + nidx * ad.rpad;
+                const uint32_t taddr = tB + lane_off + bb * static_cast<uint32_t>(rpad_max);
+                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (nidx < p.n) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&accB_empty[bb]);
+            ++units_done;
+            if (last) {
+                ok = mbar_wait(accS_full, items_done & 1u, w, 6);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                const int64_t row = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
+                float* dst = p.dS_acc + row * p.ld;
+                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tS + lane_off + c0, v);
+                    tmem_ld_wait();
+                    if (row < p.m) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(accS_empty);
+                ++items_done;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+// dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0;
+// dB_a[c, j] = bf16(dB^T_acc_a[j, c]).
+__global__ void finalize_bwd1_kernel(const float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m,
+                                     int32_t ld, const float* __restrict__ acc_base, int64_t n,
+                                     const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dbp) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t total_s = m * ld;
+    for (int64_t i = tid; i < total_s; i += stride) {
+        const int64_t t = i / ld;
+        const int c = static_cast<int>(i - t * ld);
+        const int a = rt.tile_adapter[t >> 7];
+        float v = 0.f;
+        if (a >= 0 && c < rt.ad[a].rank) v = dS_acc[i] * rt.ad[a].scale;
+        dSq[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+    }
+    for (int a = 0; a < rt.n_adapters; ++a) {
+        const AdapterDev ad = rt.ad[a];
+        const int64_t total = static_cast<int64_t>(ad.rank) * n;
+        const float* src = acc_base + ad.dB_off;
+        uint16_t* dst = dbp.p[a];
+        for (int64_t i = tid; i < total; i += stride) {
+            const int64_t c = i / n;
+            const int64_t j = i - c * n;
+            dst[i] = static_cast<uint16_t>(pack_bf16x2(src[j * ad.rpad + c], 0.f) & 0xFFFFu);
+        }
+    }
+}
+
+}  // namespace
+
+size_t dsdb_smem_bytes(const DsDbParams& p) { return 1024 + p.stages * p.stage_bytes + (2 * p.stages + 7) * 8 + 16; }
+
+cudaError_t dsdb_configure() {
+    return cudaFuncSetAttribute(dsdb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+}
+
+cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
+    dsdb_kernel<<<grid, kThreads, dsdb_smem_bytes(p), stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_bwd1(const float* dS_acc, uint16_t* dSq, int64_t m, int32_t ld, const float* acc_base,
+                                 const AdapterPtrs& dB, int64_t n, const Routing& rt, int sms, cudaStream_t stream) {
+    finalize_bwd1_kernel<<<4 * sms, 256, 0, stream>>>(dS_acc, dSq, m, ld, acc_base, n, rt, dB);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,39 @@
+// Host-side launchers of the kernels (one translation unit per kernel family).
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "plan.h"
+
+namespace lora {
+
+constexpr int kDownStages = 6;
+constexpr int kGemmStages = 4;
+
+size_t down_smem_bytes(int stages);
+cudaError_t down_configure();
+cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_finalize_s(const float* acc, uint16_t* out, int64_t m, int32_t ld, const Routing& rt, int sms,
+                              cudaStream_t stream);
+
+size_t gemm_smem_bytes();
+cudaError_t gemm_configure();
+cudaError_t launch_gemm_fwd(const GemmParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_gemm_bwd(const GemmParams& p, int grid, cudaStream_t stream);
+
+size_t dsdb_smem_bytes(const DsDbParams& p);
+cudaError_t dsdb_configure();
+cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_finalize_bwd1(const float* dS_acc, uint16_t* dSq, int64_t m, int32_t ld, const float* acc_base,
+                                 const AdapterPtrs& dB, int64_t n, const Routing& rt, int sms, cudaStream_t stream);
+
+size_t da_smem_bytes(const DaParams& p);
+cudaError_t da_configure();
+cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_finalize_da(const float* acc_base, const AdapterPtrs& dA, int64_t k, const Routing& rt, int sms,
+                               cudaStream_t stream);
+
+cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream);
+
+}  // namespace lora

@@ -1,0 +1,121 @@
+// Launch plans shared by the host driver (api.cu) and the kernels.
+//
+// Routing for the multi-adapter form travels as kernel parameters (no device
+// tables, no host->device copies): every 128-row tile carries one adapter id
+// (LoRAFusion notes, section 5 "FusedMultiLoRA": each input tile carries its
+// adapter id and that adapter's rank, scale and dropout rate).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace lora {
+
+constexpr int kTileM = 128;          // rows per routing tile (= GEMM M tile)
+constexpr int kMaxAdapters = 16;
+constexpr int kMaxTiles = 2048;      // m <= 262144
+constexpr int kMaxRank = 128;
+
+// Kernel ids for device status codes (code = id << 8 | call site).
+enum KernelId : int { kKDown = 1, kKGemmFwd = 2, kKGemmBwd = 3, kKDsDb = 4, kKDa = 5, kKDebug = 6 };
+
+struct AdapterDev {
+    int32_t rank;      // r_i
+    int32_t rpad;      // power of two >= max(16, r_i): the MMA N (or M) extent of the rank
+    uint32_t T;        // keep threshold: a 16-bit lane >= T keeps its element
+    float scale;       // alpha_i / (1 - p_i): applied to (X.*D) A and to dY B^T
+    int64_t dB_off;    // float offset of this adapter's dB^T accumulator (n x rpad)
+    int64_t dA_off;    // float offset of this adapter's dA accumulator (k x rpad)
+};
+
+struct Routing {
+    int32_t n_tiles;                         // ceil(m / 128)
+    int32_t n_active;                        // tiles that have an adapter
+    int32_t n_adapters;
+    int32_t rpad_max;                        // max rpad over adapters (16 if none)
+    int32_t adapter_begin[kMaxAdapters + 1]; // active_tiles[adapter_begin[a] .. adapter_begin[a+1]) = tiles of a
+    AdapterDev ad[kMaxAdapters];
+    int8_t tile_adapter[kMaxTiles];          // -1: no adapter
+    uint16_t active_tiles[kMaxTiles];        // tile ids grouped by adapter, ascending within a group
+};
+
+// Per-adapter output pointers for the finalize kernels.
+struct AdapterPtrs {
+    uint16_t* p[kMaxAdapters];
+};
+
+struct DevCtl {
+    int* status;        // device status word (workspace)
+    uint64_t wait_ns;   // bounded-wait limit
+};
+
+// Down-projection: S_acc[t, c] += sum_j (X .* D)[t, j] A_a[j, c] over stream-K
+// ranges of (active tile, 64-wide k-block) units.
+struct DownParams {
+    CUtensorMap mapX;                  // X: dims {k, m}, box {64, 128}, 128B swizzle
+    CUtensorMap mapA[kMaxAdapters];    // A_i: dims {r_i, k}, box {min(rpad,64), 64}, swizzle by rpad
+    Routing rt;
+    DevCtl ctl;
+    float* S_acc;                      // m x ld fp32
+    uint8_t* mask_bits;                // optional, m x k/8
+    int64_t m, k;
+    int32_t ld;                        // s_ld
+    int32_t nkb;                       // ceil(k / 64)
+    int64_t units;                     // n_active * nkb
+    uint32_t seed_lo, seed_hi;
+    int32_t stages;
+};
+
+// GEMM with the rank-r tail.
+//  forward:  Y = [X | S'] [W ; B_a]           (B operand MN-major)
+//  backward: dX = dY W^T + D .* (dSq A_a^T)   (B operand K-major; second accumulator)
+struct GemmParams {
+    CUtensorMap mapA;                  // fwd: X {k, m}; bwd: dY {n, m}; box {64, 128}
+    CUtensorMap mapB;                  // fwd: W {n, k} box {64, 64}; bwd: W {n, k} box {64, 256}
+    CUtensorMap mapTA;                 // tail A: fwd S' / bwd dSq, {s_ld, m}, box {64, 128}
+    CUtensorMap mapTB[kMaxAdapters];   // tail B: fwd B_i {n, r_i} box {64, 64}; bwd A_i {r_i, k} box {64, 256}
+    Routing rt;
+    DevCtl ctl;
+    uint16_t* out;                     // Y (m x n) or dX (m x k), bf16
+    int64_t M, N, K;                   // GEMM sizes: fwd (m, n, k), bwd (m, k, n)
+    int32_t n_mtiles, n_ntiles, nkb;
+    int32_t group_m;                   // rasterisation: m-tiles per group
+    uint32_t seed_lo, seed_hi;
+};
+
+// dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,
+//   acc_dS[tile]  += dY_tile B_a^T        (accumulated over the item's n-blocks)
+//   acc_dBt[nblk]  = dY_tile^T S'_tile    (flushed per unit)
+struct DsDbParams {
+    CUtensorMap mapDY;                 // dY {n, m}, box {64, 128}, 128B swizzle
+    CUtensorMap mapB[kMaxAdapters];    // B_i {n, r_i}, box {64, rpad}, 128B swizzle (K-major, K = n)
+    CUtensorMap mapS[kMaxAdapters];    // S' {s_ld, m}, box {min(rpad,64), 128}, swizzle by rpad (MN-major)
+    Routing rt;
+    DevCtl ctl;
+    float* dS_acc;                     // m x ld fp32
+    float* acc_base;                   // adapter accumulators (dB_off)
+    int64_t m, n;
+    int32_t ld;
+    int32_t nnb;                       // ceil(n / 128)
+    int64_t units;                     // n_active * nnb
+    int32_t stages;
+    uint32_t stage_bytes, off_b, off_s; // stage layout
+};
+
+// dA = (X .* D)^T dSq per adapter: per (adapter, 128-feature block, tile) unit.
+struct DaParams {
+    CUtensorMap mapX;                  // X {k, m}, box {64, 128}, 128B swizzle
+    CUtensorMap mapD[kMaxAdapters];    // dSq {s_ld, m}, box {min(rpad,64), 128}, swizzle by rpad (MN-major)
+    Routing rt;
+    DevCtl ctl;
+    float* acc_base;                   // adapter accumulators (dA_off)
+    int64_t m, k;
+    int32_t nfb;                       // ceil(k / 128)
+    int64_t units;                     // nfb * n_active
+    int64_t unit_begin[kMaxAdapters + 1];  // first unit of each adapter
+    uint32_t seed_lo, seed_hi;
+    int32_t stages;
+    uint32_t stage_bytes, off_d;
+};
+
+}  // namespace lora

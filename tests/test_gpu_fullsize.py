@@ -1,0 +1,110 @@
+"""GPU parity at the benchmark sizes, in the launch configuration the benchmark times.
+
+The oracle computes, in fp64 on the host: the full keep mask, S, dS-derived
+dA and dB (all O(m r (k + n))), and Y / dX on a sample of rows (256 random rows
+plus two whole 128-row tiles), which it computes one row at a time.
+"""
+import numpy as np
+import pytest
+
+from tests.gpu_helpers import assert_close, host_f64, to_dev, torch
+
+from lora_fine_tuning_gb300 import synth
+from oracle import lora_oracle as O
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from lora_fine_tuning_gb300 import api  # noqa: E402
+
+
+def sample_rows(m, seed):
+    rng = np.random.default_rng(seed)
+    rows = set(rng.choice(m, size=min(256, m), replace=False).tolist())
+    rows.update(range(0, min(128, m)))                    # first tile
+    rows.update(range(max(0, m - 128), m))                # last tile
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", ["llama8b_up", "llama70b_o_r64"])
+def test_single_adapter_full_size(name):
+    cfg = synth.WORKLOADS[name]
+    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
+    raw = synth.layer_inputs(seed, m, k, n, r)
+    X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
+    Y, S, mask = api.lora_fwd(X, W, A, B, alpha, p, seed, want_mask=True)
+    dX, dA, dB = api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed)
+    torch.cuda.synchronize()
+    assert api.lora_device_status(api.workspace(m, k, n, r)) == 0
+
+    Xo = O.bf16_to_f64(raw["X"])
+    Ao, Bo = O.bf16_to_f64(raw["A"]), O.bf16_to_f64(raw["B"])
+    T, q = O.dropout_threshold(p), O.dropout_scale(p)
+    D = O.keep_mask(seed, np.arange(m), k, T)
+    np.testing.assert_array_equal(mask.cpu().numpy(), O.pack_mask_bits(D))
+    Xhat = Xo * D * q
+    del D
+    Sr = Xhat @ Ao
+    assert_close("S_saved", host_f64(S), alpha * Sr)
+    dYo = O.bf16_to_f64(raw["dY"])
+    dSr = alpha * (dYo @ Bo.T)
+    assert_close("dB", host_f64(dB), alpha * (Sr.T @ dYo))
+    assert_close("dA", host_f64(dA), Xhat.T @ dSr)
+    del Xhat
+
+    rows = sample_rows(m, seed)
+    Wo = O.bf16_to_f64(raw["W"])
+    Yr, _, _ = O.lora_forward(Xo[rows], Wo, Ao, Bo, alpha, p, seed, rows=rows)
+    assert_close("Y[rows]", host_f64(Y[torch.from_numpy(rows).cuda()]), Yr)
+    dXr, _, _, _ = O.lora_backward(dYo[rows], Xo[rows], Wo, Ao, Bo, alpha, p, seed, rows=rows)
+    assert_close("dX[rows]", host_f64(dX[torch.from_numpy(rows).cuda()]), dXr)
+
+
+def test_multi_adapter_full_size():
+    w = synth.MULTI_WORKLOAD
+    k, n, seed, specs = w["k"], w["n"], w["seed"], w["specs"]
+    batch = synth.packed_batch(seed, w["total_rows"], len(specs))
+    raw = synth.multi_inputs(seed, k, n, specs, batch)
+    X, W, dY = (to_dev(raw[x]) for x in ("X", "W", "dY"))
+    adapters = [api.Adapter(A=to_dev(A), B=to_dev(B), alpha=s.alpha, p=s.p) for (A, B), s in zip(raw["adapters"], specs)]
+    Y, S, mask = api.multi_lora_fwd(X, W, adapters, batch.segments, seed, want_mask=True)
+    dX = api.multi_lora_bwd(dY, X, W, adapters, batch.segments, seed, S)
+    torch.cuda.synchronize()
+
+    m = batch.m
+    Xo, dYo = O.bf16_to_f64(raw["X"]), O.bf16_to_f64(raw["dY"])
+    owner = O.row_adapters(batch.segments, m, len(specs))
+    mbits = mask.cpu().numpy()
+    S_host = host_f64(S)
+    for i, ((A, B), s) in enumerate(zip(raw["adapters"], specs)):
+        sel = np.nonzero(owner == i)[0]
+        Ao, Bo = O.bf16_to_f64(A), O.bf16_to_f64(B)
+        if sel.size == 0:
+            assert not host_f64(adapters[i].dA).any() and not host_f64(adapters[i].dB).any()
+            continue
+        D = O.keep_mask(seed, sel, k, O.dropout_threshold(s.p))
+        np.testing.assert_array_equal(mbits[sel], O.pack_mask_bits(D))
+        Xhat = Xo[sel] * D * O.dropout_scale(s.p)
+        Sr = Xhat @ Ao
+        assert_close(f"S[{i}]", S_host[sel, :s.rank], s.alpha * Sr)
+        dSr = s.alpha * (dYo[sel] @ Bo.T)
+        assert_close(f"dB[{i}]", host_f64(adapters[i].dB), s.alpha * (Sr.T @ dYo[sel]))
+        assert_close(f"dA[{i}]", host_f64(adapters[i].dA), Xhat.T @ dSr)
+
+    rows = sample_rows(m, seed)
+    Wo = O.bf16_to_f64(raw["W"])
+    ads_o = [dict(A=O.bf16_to_f64(A), B=O.bf16_to_f64(B), alpha=s.alpha, p=s.p)
+             for (A, B), s in zip(raw["adapters"], specs)]
+    Yr, _, _ = O.multi_lora_forward(Xo[rows], Wo, ads_o, batch.segments, seed, rows=rows)
+    assert_close("Y[rows]", host_f64(Y[torch.from_numpy(rows).cuda()]), Yr)
+    # dX on the sampled rows: base part plus each row's own adapter branch
+    dXr = dYo[rows] @ Wo.T
+    for i, ad in enumerate(ads_o):
+        pick = np.nonzero(owner[rows] == i)[0]
+        if pick.size:
+            dXb, _, _, _ = O.lora_branch_backward(dYo[rows[pick]], Xo[rows[pick]], ad["A"], ad["B"], ad["alpha"],
+                                                  ad["p"], seed, rows[pick])
+            dXr[pick] += dXb
+    assert_close("dX[rows]", host_f64(dX[torch.from_numpy(rows).cuda()]), dXr)
