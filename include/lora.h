@@ -159,6 +159,10 @@ lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void*
 
 const char* lora_status_string(lora_status s);
 
+/* Host only: the CUDA error text behind the calling thread's last LORA_ECUDA
+ * (a static string; "no error" if none occurred). */
+const char* lora_last_error_string(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -26,6 +26,13 @@ struct DeviceState {
 };
 
 std::mutex g_mu;
+thread_local const char* g_last_error = "no error";
+
+bool cuda_ok(cudaError_t e) {
+    if (e == cudaSuccess) return true;
+    g_last_error = cudaGetErrorString(e);
+    return false;
+}
 DeviceState g_dev[64];
 uint64_t g_wait_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -38,25 +45,26 @@ lora_status device_setup(int* sms_out) {
     if (!d.ready) {
         d.ready = true;
         int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        if (!cuda_ok(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) ||
+            !cuda_ok(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) ||
+            !cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev))) {
             d.status = LORA_ECUDA;
         } else if (major != 10 || minor != 3) {
             d.status = LORA_EARCH;
         } else {
             d.sms = sms;
-            if (down_configure() != cudaSuccess || gemm_configure() != cudaSuccess ||
-                dsdb_configure() != cudaSuccess || da_configure() != cudaSuccess)
+            if (!cuda_ok(down_configure()) || !cuda_ok(gemm_configure()) || !cuda_ok(dsdb_configure()) ||
+                !cuda_ok(da_configure()))
                 d.status = LORA_ECUDA;
         }
         if (d.status == LORA_OK && g_encode == nullptr) {
             void* fn = nullptr;
             cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                    cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || fn == nullptr)
+            if (!cuda_ok(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q)) ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                if (q != cudaDriverEntryPointSuccess) g_last_error = "cuTensorMapEncodeTiled entry point not found";
                 d.status = LORA_ECUDA;
+            }
             else
                 g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
@@ -74,9 +82,11 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
     cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) g_last_error = "cuTensorMapEncodeTiled rejected a tensor map";
+    return r == CUDA_SUCCESS;
 }
 
 CUtensorMapSwizzle rank_swizzle_host(int rpad) {
@@ -251,9 +261,9 @@ lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_se
 
 DevCtl ctl_of(const Call& c) { return DevCtl{reinterpret_cast<int*>(c.ws + c.L.status), g_wait_ns}; }
 
-#define LORA_CUDA(expr)                                  \
-    do {                                                 \
-        if ((expr) != cudaSuccess) return LORA_ECUDA;    \
+#define LORA_CUDA(expr)                          \
+    do {                                         \
+        if (!cuda_ok(expr)) return LORA_ECUDA;   \
     } while (0)
 
 lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const lora_adapter* ads, uint64_t seed,
@@ -360,7 +370,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             p.off_b = 32768;
             p.off_s = p.off_b + 2 * 128 * rpm;
             p.stage_bytes = p.off_s + 256 * rpm;
-            p.stages = static_cast<int32_t>(std::min<size_t>(8, (220 * 1024) / p.stage_bytes));
+            p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
             const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
             LORA_CUDA(launch_dsdb(p, grid, c.stream));
         }
@@ -422,7 +432,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
             p.off_d = 32768;
             p.stage_bytes = p.off_d + 256 * rpm;
-            p.stages = static_cast<int32_t>(std::min<size_t>(8, (220 * 1024) / p.stage_bytes));
+            p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
             const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
             LORA_CUDA(launch_da(p, grid, c.stream));
         }
@@ -542,9 +552,11 @@ lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void*
     lora_status st = device_setup(&sms);
     if (st) return st;
     DevCtl ctl{static_cast<int*>(workspace), g_wait_ns};
-    if (launch_stuck_wait(ctl, static_cast<cudaStream_t>(stream)) != cudaSuccess) return LORA_ECUDA;
+    if (!cuda_ok(launch_stuck_wait(ctl, static_cast<cudaStream_t>(stream)))) return LORA_ECUDA;
     return LORA_OK;
 }
+
+const char* lora_last_error_string(void) { return g_last_error; }
 
 const char* lora_status_string(lora_status s) {
     switch (s) {

@@ -258,7 +258,7 @@ __global__ void stuck_wait_kernel(DevCtl ctl) {
 size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 5) * 8 + 16; }
 
 cudaError_t da_configure() {
-    return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream) {

@@ -262,7 +262,7 @@ __global__ void finalize_bwd1_kernel(const float* __restrict__ dS_acc, uint16_t*
 size_t dsdb_smem_bytes(const DsDbParams& p) { return 1024 + p.stages * p.stage_bytes + (2 * p.stages + 7) * 8 + 16; }
 
 cudaError_t dsdb_configure() {
-    return cudaFuncSetAttribute(dsdb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    return cudaFuncSetAttribute(dsdb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {

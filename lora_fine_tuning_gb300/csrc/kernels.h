@@ -10,6 +10,11 @@ namespace lora {
 
 constexpr int kDownStages = 6;
 constexpr int kGemmStages = 4;
+// Dynamic shared memory a kernel may request; leaves room for its few bytes
+// of static shared memory under the 227 KB per-block limit.
+constexpr int kMaxDynSmem = 225 * 1024;
+// Stage ring budget of the rank-r kernels (stages * stage bytes).
+constexpr int kStageBudget = 220 * 1024;
 
 size_t down_smem_bytes(int stages);
 cudaError_t down_configure();

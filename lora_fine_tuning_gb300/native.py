@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
 # Symbols include/lora.h declares, in declaration order.
 EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd", "lora_tile_table",
             "lora_keep_threshold", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
-            "lora_status_string"]
+            "lora_status_string", "lora_last_error_string"]
 
 
 class LoraAdapter(ctypes.Structure):
@@ -34,7 +34,13 @@ class LoraSegment(ctypes.Structure):
 
 class LoraError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: {status_string(status)}")
+        detail = ""
+        if status == 5:
+            try:
+                detail = f" ({lib().lora_last_error_string().decode()})"
+            except Exception:
+                pass
+        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}: {status_string(status)}{detail}")
         self.status = status
 
 
@@ -66,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "lora_set_wait_limit_ns": (None, [u64]),
             "lora_debug_stuck_wait": (i32, [vp, sz, vp]),
             "lora_status_string": (ctypes.c_char_p, [i32]),
+            "lora_last_error_string": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
