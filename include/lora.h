@@ -159,6 +159,19 @@ lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void*
 
 const char* lora_status_string(lora_status s);
 
+/* Measurement: between lora_timing_begin() and lora_timing_end(), every
+ * kernel (and workspace memset) the library enqueues is bracketed by CUDA
+ * events on its own stream.  lora_timing_end() waits for those events and
+ * fills, for each kind i < n_kinds (see lora_kernel_name), the summed device
+ * time in ms and the number of launches.  Kinds: 0 down-projection,
+ * 1 finalize S, 2 forward GEMM, 3 dS/dB, 4 finalize dS/dB, 5 backward GEMM,
+ * 6 dA, 7 finalize dA, 8 workspace memset.  Host-side cost: two event
+ * records per launch. */
+enum { LORA_KERNEL_KINDS = 9 };
+lora_status lora_timing_begin(void);
+lora_status lora_timing_end(float* total_ms, int32_t* launches, int32_t n_kinds);
+const char* lora_kernel_name(int32_t kind);
+
 /* Host only: the CUDA error text behind the calling thread's last LORA_ECUDA
  * (a static string; "no error" if none occurred). */
 const char* lora_last_error_string(void);

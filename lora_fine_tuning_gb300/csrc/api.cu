@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kernels.h"
 #include "lora.h"
@@ -36,6 +37,48 @@ bool cuda_ok(cudaError_t e) {
 DeviceState g_dev[64];
 uint64_t g_wait_ns = 2000000000ull;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// ---------------------------------------------------------------------------
+// optional per-kernel timing (measurement tools): events around each launch
+// ---------------------------------------------------------------------------
+
+enum Kind : int {
+    kDownProj = 0, kFinalizeS, kGemmFwd, kDsDb, kFinalizeBwd1, kGemmBwd, kDa, kFinalizeDa, kMemset, kKinds
+};
+const char* const kKindNames[kKinds] = {"down_proj", "finalize_s", "gemm_fwd", "ds_db", "finalize_bwd1",
+                                        "gemm_bwd", "da", "finalize_da", "memset"};
+
+struct TimingRec {
+    int kind;
+    cudaEvent_t a, b;
+};
+std::mutex g_timing_mu;
+bool g_timing_on = false;
+std::vector<TimingRec> g_timing;
+std::vector<cudaEvent_t> g_event_pool;
+size_t g_pool_next = 0;
+
+cudaEvent_t pool_event() {
+    if (g_pool_next == g_event_pool.size()) {
+        cudaEvent_t e = nullptr;
+        if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+        g_event_pool.push_back(e);
+    }
+    return g_event_pool[g_pool_next++];
+}
+
+// Runs `launch` (which enqueues work on `s`); when timing is on, brackets it with events.
+template <class F>
+cudaError_t timed(int kind, cudaStream_t s, F&& launch) {
+    if (!g_timing_on) return launch();
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    cudaEvent_t a = pool_event(), b = pool_event();
+    if (a) cudaEventRecord(a, s);
+    const cudaError_t e = launch();
+    if (b) cudaEventRecord(b, s);
+    if (a && b) g_timing.push_back(TimingRec{kind, a, b});
+    return e;
+}
 
 lora_status device_setup(int* sms_out) {
     int dev = 0;
@@ -274,7 +317,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     float* s_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
 
     if (nad > 0) {
-        LORA_CUDA(cudaMemsetAsync(s_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream));
+        LORA_CUDA(timed(kMemset, c.stream, [&] { return cudaMemsetAsync(s_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream); }));
         if (c.rt.n_active > 0) {
             static DownParams p;  // large: keep it off the stack
             std::memset(&p, 0, sizeof(p));
@@ -298,9 +341,9 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
             p.seed_hi = seed_hi;
             p.stages = kDownStages;
             const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(launch_down(p, grid, c.stream));
+            LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
         }
-        LORA_CUDA(launch_finalize_s(s_acc, S_saved, m, c.s_ld, c.rt, c.sms, c.stream));
+        LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(s_acc, S_saved, m, c.s_ld, c.rt, c.sms, c.stream); }));
     }
 
     static GemmParams g;
@@ -326,7 +369,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     g.seed_lo = seed_lo;
     g.seed_hi = seed_hi;
     const int tiles = g.n_mtiles * g.n_ntiles;
-    LORA_CUDA(launch_gemm_fwd(g, std::min(tiles, c.sms), c.stream));
+    LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm_fwd(g, std::min(tiles, c.sms), c.stream); }));
     return LORA_OK;
 }
 
@@ -344,8 +387,10 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
     }
 
     if (nad > 0) {
-        if (m > 0) LORA_CUDA(cudaMemsetAsync(ds_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream));
-        LORA_CUDA(cudaMemsetAsync(acc, 0, c.L.acc_floats * 4, c.stream));
+        if (m > 0)
+            LORA_CUDA(timed(kMemset, c.stream,
+                            [&] { return cudaMemsetAsync(ds_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream); }));
+        LORA_CUDA(timed(kMemset, c.stream, [&] { return cudaMemsetAsync(acc, 0, c.L.acc_floats * 4, c.stream); }));
         if (c.rt.n_active > 0) {
             static DsDbParams p;
             std::memset(&p, 0, sizeof(p));
@@ -372,9 +417,10 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             p.stage_bytes = p.off_s + 256 * rpm;
             p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
             const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(launch_dsdb(p, grid, c.stream));
+            LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
         }
-        LORA_CUDA(launch_finalize_bwd1(ds_acc, dsq, m, c.s_ld, acc, dBp, n, c.rt, c.sms, c.stream));
+        LORA_CUDA(timed(kFinalizeBwd1, c.stream,
+                        [&] { return launch_finalize_bwd1(ds_acc, dsq, m, c.s_ld, acc, dBp, n, c.rt, c.sms, c.stream); }));
     }
 
     if (m > 0) {
@@ -401,7 +447,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         g.seed_lo = seed_lo;
         g.seed_hi = seed_hi;
         const int tiles = g.n_mtiles * g.n_ntiles;
-        LORA_CUDA(launch_gemm_bwd(g, std::min(tiles, c.sms), c.stream));
+        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm_bwd(g, std::min(tiles, c.sms), c.stream); }));
     }
 
     if (nad > 0) {
@@ -434,9 +480,9 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             p.stage_bytes = p.off_d + 256 * rpm;
             p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
             const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(launch_da(p, grid, c.stream));
+            LORA_CUDA(timed(kDa, c.stream, [&] { return launch_da(p, grid, c.stream); }));
         }
-        LORA_CUDA(launch_finalize_da(acc, dAp, k, c.rt, c.sms, c.stream));
+        LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(acc, dAp, k, c.rt, c.sms, c.stream); }));
     }
     return LORA_OK;
 }
@@ -557,6 +603,41 @@ lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void*
 }
 
 const char* lora_last_error_string(void) { return g_last_error; }
+
+lora_status lora_timing_begin(void) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    g_timing.clear();
+    g_pool_next = 0;
+    g_timing_on = true;
+    return LORA_OK;
+}
+
+lora_status lora_timing_end(float* total_ms, int32_t* launches, int32_t n_kinds) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    g_timing_on = false;
+    if (!total_ms || !launches || n_kinds < 0) return LORA_EINVAL;
+    for (int i = 0; i < n_kinds; ++i) {
+        total_ms[i] = 0.f;
+        launches[i] = 0;
+    }
+    lora_status st = LORA_OK;
+    for (const TimingRec& r : g_timing) {
+        float ms = 0.f;
+        if (!cuda_ok(cudaEventSynchronize(r.b)) || !cuda_ok(cudaEventElapsedTime(&ms, r.a, r.b))) {
+            st = LORA_ECUDA;
+            continue;
+        }
+        if (r.kind < n_kinds) {
+            total_ms[r.kind] += ms;
+            launches[r.kind] += 1;
+        }
+    }
+    g_timing.clear();
+    g_pool_next = 0;
+    return st;
+}
+
+const char* lora_kernel_name(int32_t kind) { return (kind >= 0 && kind < kKinds) ? kKindNames[kind] : "unknown"; }
 
 const char* lora_status_string(lora_status s) {
     switch (s) {

@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
 # Symbols include/lora.h declares, in declaration order.
 EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd", "lora_tile_table",
             "lora_keep_threshold", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
-            "lora_status_string", "lora_last_error_string"]
+            "lora_status_string", "lora_timing_begin", "lora_timing_end", "lora_kernel_name",
+            "lora_last_error_string"]
 
 
 class LoraAdapter(ctypes.Structure):
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
             "lora_debug_stuck_wait": (i32, [vp, sz, vp]),
             "lora_status_string": (ctypes.c_char_p, [i32]),
             "lora_last_error_string": (ctypes.c_char_p, []),
+            "lora_timing_begin": (i32, []),
+            "lora_timing_end": (i32, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32), i32]),
+            "lora_kernel_name": (ctypes.c_char_p, [i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -116,3 +120,18 @@ def keep_threshold(p: float) -> int:
     T = ctypes.c_uint32(0)
     check("lora_keep_threshold", lib().lora_keep_threshold(ctypes.c_float(p), ctypes.byref(T)))
     return T.value
+
+
+KERNEL_KINDS = 9
+
+
+def timing_begin() -> None:
+    check("lora_timing_begin", lib().lora_timing_begin())
+
+
+def timing_end() -> dict:
+    """{kernel name: (total device ms, launches)} for the launches since timing_begin()."""
+    ms = (ctypes.c_float * KERNEL_KINDS)()
+    n = (ctypes.c_int32 * KERNEL_KINDS)()
+    check("lora_timing_end", lib().lora_timing_end(ms, n, KERNEL_KINDS))
+    return {lib().lora_kernel_name(i).decode(): (float(ms[i]), int(n[i])) for i in range(KERNEL_KINDS) if n[i]}
