@@ -135,6 +135,32 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
                            int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* lora_fwd for callers that cannot allocate device memory (no counterpart in
+ * the LoRAFusion write-ups; it only changes where the scratch lives).
+ * Some callers have no way to hand the library a workspace: a plugin whose
+ * host application plans every device buffer ahead of time and offers none
+ * to extensions, or a runtime that forbids allocation on its compute path.
+ * This entry point takes the same arguments as lora_fwd minus the workspace
+ * and uses a file-scope device array of LORA_STATIC_SCRATCH_BYTES (8 MiB)
+ * inside the library instead; every GPU that loads the library keeps that
+ * array until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *  - Sizes whose scratch need (lora_workspace_size(m, k, n, r, 1)) exceeds
+ *    8 MiB are rejected with LORA_EWORKSPACE and lora_last_error_string()
+ *    says why.  For example m = 8192, k = 4096, n = 14336, r = 16 needs 2 MB.
+ *  - The first call on each device looks up the array's device address and
+ *    clears its status word, on `stream`; make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; each call clears what it needs at zero.  Calls whose work can
+ *    overlap on the GPU (different streams, no ordering) race on the array.
+ *  - Bounded-wait timeouts are recorded in the array's status word, which no
+ *    entry point reads back. */
+enum { LORA_STATIC_SCRATCH_BYTES = 8 << 20 };
+lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
+                                    float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r,
+                                    lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits, void* stream);
+
 /* Host only, no GPU needed: the routing table.  tile_adapter[i] (i < ceil(m/128))
  * receives the adapter of tile i, -1 where no segment covers it. */
 lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, int32_t n_adapters, int64_t m,

@@ -489,6 +489,14 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
 
 std::mutex g_call_mu;  // the static parameter blocks above are shared
 
+// Scratch for lora_fwd_static_scratch, for callers that cannot hand the
+// library any device memory of their own.  Every GPU that loads the library
+// holds this array until the process exits; all calls on one GPU share it.
+constexpr size_t kStaticScratchBytes = 8u << 20;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+void* g_static_scratch_ptr[64] = {};   // device address of the array, per device
+std::mutex g_static_mu;
+
 }  // namespace
 }  // namespace lora
 
@@ -552,6 +560,33 @@ lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
     lora_segment seg{0, m, 0, 0};
     return multi_lora_bwd(dY, X, W, &ad, 1, &seg, m > 0 ? 1 : 0, seed, m, k, n, S_saved, dX, workspace,
                           workspace_bytes, stream);
+}
+
+lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
+                                    float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r,
+                                    lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits, void* stream) {
+    const size_t need = lora_workspace_size(m, k, n, r, 1);
+    if (need > kStaticScratchBytes) {
+        g_last_error = "lora_fwd_static_scratch: these sizes need more scratch than the 8 MiB static buffer";
+        return LORA_EWORKSPACE;
+    }
+    int dev = 0;
+    if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 64) return LORA_ECUDA;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        if (g_static_scratch_ptr[dev] == nullptr) {
+            // Once per device, with that device current: the host name of the
+            // array is only a stand-in, so look up its device address.
+            void* ptr = nullptr;
+            if (!cuda_ok(cudaGetSymbolAddress(&ptr, g_static_scratch))) return LORA_ECUDA;
+            // The device status word must start at zero.
+            if (!cuda_ok(cudaMemsetAsync(ptr, 0, kAlign, static_cast<cudaStream_t>(stream)))) return LORA_ECUDA;
+            g_static_scratch_ptr[dev] = ptr;
+        }
+        scratch = g_static_scratch_ptr[dev];
+    }
+    return lora_fwd(X, W, A, B, alpha, p, seed, m, k, n, r, Y, S_saved, mask_bits, scratch, kStaticScratchBytes, stream);
 }
 
 lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, int32_t n_adapters, int64_t m,

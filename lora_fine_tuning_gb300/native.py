@@ -17,7 +17,8 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
                 5: "LORA_ECUDA", 6: "LORA_EWORKSPACE", 7: "LORA_EDEVICE_TIMEOUT", 8: "LORA_ETABLE"}
 
 # Symbols include/lora.h declares, in declaration order.
-EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd", "lora_tile_table",
+EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd",
+            "lora_fwd_static_scratch", "lora_tile_table",
             "lora_keep_threshold", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
             "lora_status_string", "lora_timing_begin", "lora_timing_end", "lora_kernel_name",
             "lora_last_error_string"]
@@ -66,6 +67,7 @@ def lib() -> ctypes.CDLL:
                                      i64, i64, i64, vp, vp, vp, vp, sz, vp]),
             "multi_lora_bwd": (i32, [vp, vp, vp, ctypes.POINTER(LoraAdapter), i32, ctypes.POINTER(LoraSegment), i32,
                                      u64, i64, i64, i64, vp, vp, vp, sz, vp]),
+            "lora_fwd_static_scratch": (i32, [vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp]),
             "lora_tile_table": (i32, [ctypes.POINTER(LoraSegment), i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                       i64]),
             "lora_keep_threshold": (i32, [f32, ctypes.POINTER(ctypes.c_uint32)]),
