@@ -435,6 +435,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--m", type=int, default=None, help="override the workload's token count (profiling runs)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline leg")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -443,6 +444,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.m is not None:
+        synth.WORKLOADS[args.workload] = dict(synth.WORKLOADS[args.workload], m=args.m)
     if args.impl == "reference":
         run_reference(args)
     else:
