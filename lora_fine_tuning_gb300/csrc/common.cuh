@@ -269,24 +269,40 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Philox4x32-10 keep mask (Salmon, Moraes, Dror, Shaw, SC'11)
 // ---------------------------------------------------------------------------
 
-// Counter (c0, c1, 0, 0), key (k0, k1); ten rounds, key bumped by the Weyl
-// increments between rounds.
-__device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+// Round keys of one seed: round r uses (k0 + r*W0, k1 + r*W1).
+struct PhiloxKeys {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint32_t k0, uint32_t k1) {
+    PhiloxKeys K;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        K.k0[r] = k0 + static_cast<uint32_t>(r) * 0x9E3779B9u;
+        K.k1[r] = k1 + static_cast<uint32_t>(r) * 0xBB67AE85u;
+    }
+    return K;
+}
+
+// Counter (c0, c1, 0, 0); ten rounds.  Each round is two 32x32->64 products
+// (one IMAD.WIDE each: high and low words come out as a register pair) and
+// two three-input XORs.
+__device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, const PhiloxKeys& K) {
     uint32_t x0 = c0, x1 = c1, x2 = 0u, x3 = 0u;
 #pragma unroll
     for (int r = 0; r < 10; ++r) {
-        const uint32_t lo0 = 0xD2511F53u * x0;
-        const uint32_t hi0 = __umulhi(0xD2511F53u, x0);
-        const uint32_t lo1 = 0xCD9E8D57u * x2;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, x2);
-        x0 = hi1 ^ x1 ^ k0;
-        x1 = lo1;
-        x2 = hi0 ^ x3 ^ k1;
-        x3 = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
+        const uint64_t p0 = static_cast<uint64_t>(x0) * 0xD2511F53u;
+        const uint64_t p1 = static_cast<uint64_t>(x2) * 0xCD9E8D57u;
+        x0 = static_cast<uint32_t>(p1 >> 32) ^ x1 ^ K.k0[r];
+        x1 = static_cast<uint32_t>(p1);
+        x2 = static_cast<uint32_t>(p0 >> 32) ^ x3 ^ K.k1[r];
+        x3 = static_cast<uint32_t>(p0);
     }
     return make_uint4(x0, x1, x2, x3);
+}
+
+__device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0, uint32_t k1) {
+    return philox_10(c0, c1, philox_keys(k0, k1));
 }
 
 // One Philox word covers two bf16 elements: the low 16-bit lane decides the
@@ -296,6 +312,13 @@ __device__ __forceinline__ uint32_t keep_pair_mask(uint32_t w, uint32_t T) {
     const uint32_t lo = ((w & 0xFFFFu) >= T) ? 0x0000FFFFu : 0u;
     const uint32_t hi = ((w >> 16) >= T) ? 0xFFFF0000u : 0u;
     return lo | hi;
+}
+
+// Zeroes the dropped elements of a packed bf16 pair.
+__device__ __forceinline__ uint32_t apply_keep(uint32_t data, uint32_t w, uint32_t T) {
+    if ((w & 0xFFFFu) < T) data &= 0xFFFF0000u;
+    if ((w >> 16) < T) data &= 0x0000FFFFu;
+    return data;
 }
 
 // Eight keep bits (bit e = element e of the 8-group).

@@ -5,7 +5,7 @@
 // it: dA = X_hat^T dS = (X .* D)^T (q dS) = (X .* D)^T dSq.
 // Each unit is (adapter a, 128-feature block, one of a's 128-row tiles): two
 // TMA boxes of X (128 tokens x 64 features, 128B swizzle) plus the tile's dSq
-// rows.  Warps 2..5 zero the dropped X elements in shared memory (Philox,
+// rows.  Warps 2..9 zero the dropped X elements in shared memory (Philox,
 // exactly as the forward), warp 1 issues tcgen05.mma with both operands
 // MN-major (M = 128 features, N = rank, K = 128 tokens) accumulating over a
 // CTA's run of tiles of one (adapter, feature block), and the run's partial is
@@ -17,7 +17,8 @@ namespace lora {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 mask (2..5 also epilogue)
+constexpr int kMaskThreads = 256;
 constexpr uint32_t kXBytes = 2u * 128u * 128u;   // 128 tokens x 128 features
 
 struct DaUnit {
@@ -60,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&masked[s], 128);
+            mbar_init(&masked[s], kMaskThreads);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -150,8 +151,15 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        const int et = threadIdx.x - 64;
+        // warps 2..9 mask the two staged X boxes: thread -> (row, box) walks
+        // the 8 chunks of one row of one box.  Warps 2..5 also run the
+        // epilogue (TMEM lane quadrant = warp % 4).
+        const int mt = threadIdx.x - 64;
+        const int row = mt & 127;
+        const int h = mt >> 7;
+        const bool epilogue = warp < 6;
         const int quad = warp & 3;
+        const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
@@ -162,29 +170,24 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (ad.T != 0u) {
-                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
-#pragma unroll 2
-                for (int i = 0; i < 16; ++i) {
-                    const int h = i >> 3;
-                    const int ch = et + 128 * (i & 7);
-                    const int row = ch >> 3;
-                    const int c16 = ch & 7;
-                    const uint32_t addr = st + h * 16384 + row * 128 + ((c16 ^ (row & 7)) << 4);
-                    const int64_t t = static_cast<int64_t>(d.tile) * kTileM + row;
-                    const int64_t j0 = static_cast<int64_t>(d.fb) * 128 + h * 64 + c16 * 8;
-                    const uint4 wv = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(j0 >> 3), p.seed_lo,
-                                               p.seed_hi);
+                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + h * 16384 + row * 128;
+                const uint32_t t = static_cast<uint32_t>(static_cast<int64_t>(d.tile) * kTileM + row);
+                const uint32_t g0 = static_cast<uint32_t>(d.fb * 16 + h * 8);
+#pragma unroll
+                for (int c16 = 0; c16 < 8; ++c16) {
+                    const uint4 wv = philox_10(t, g0 + c16, keys);
+                    const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
                     uint4 v = lds128(addr);
-                    v.x &= keep_pair_mask(wv.x, ad.T);
-                    v.y &= keep_pair_mask(wv.y, ad.T);
-                    v.z &= keep_pair_mask(wv.z, ad.T);
-                    v.w &= keep_pair_mask(wv.w, ad.T);
+                    v.x = apply_keep(v.x, wv.x, ad.T);
+                    v.y = apply_keep(v.y, wv.y, ad.T);
+                    v.z = apply_keep(v.z, wv.z, ad.T);
+                    v.w = apply_keep(v.w, wv.w, ad.T);
                     sts128(addr, v);
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&masked[s]);
-            if (last) {
+            if (last && epilogue) {
                 const uint32_t b = use & 1u;
                 ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -206,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
-                ++use;
             }
+            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }

@@ -5,9 +5,10 @@
 // article (juhe.plus) section 4.1 lists it as forward step ①.  Here:
 //  - warp 0 streams X tiles (128 x 64, TMA, 128B swizzle) and the matching
 //    64-row block of A_a into a ring of shared-memory stages;
-//  - warps 2..5 regenerate the keep mask with Philox4x32-10 and zero the
+//  - warps 2..9 regenerate the keep mask with Philox4x32-10 and zero the
 //    dropped elements in place (16 bytes = 8 features = one Philox call per
-//    access), then hand the stage to the MMA warp;
+//    access; each thread walks one row, so the counter's row word is shared),
+//    then hand the stage to the MMA warp;
 //  - warp 1 issues tcgen05.mma (M = 128 tokens, N = rank, K = 64 per stage)
 //    into a double-buffered TMEM accumulator;
 //  - at the end of each tile range, warps 2..5 read TMEM and add the fp32
@@ -21,7 +22,8 @@ namespace lora {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 mask (2..5 also epilogue)
+constexpr int kMaskThreads = 256;
 constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16
 constexpr uint32_t kABytes = 16384u;        // up to 64 rows x 128 bf16
 constexpr uint32_t kStageBytes = kXBytes + kABytes;
@@ -48,7 +50,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&masked[s], 128);
+            mbar_init(&masked[s], kMaskThreads);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -146,9 +148,16 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // warps 2..5: mask + epilogue.  TMEM lane quadrant = warp % 4.
-        const int et = threadIdx.x - 64;
+        // warps 2..9 mask the staged X tile: thread -> (row, half) covers the
+        // four 16-byte chunks [4*half, 4*half + 4) of one row, so the Philox
+        // counter word is the row for all of them.  Warps 2..5 also run the
+        // epilogue (TMEM lane quadrant = warp % 4).
+        const int mt = threadIdx.x - 64;
+        const int row = mt & 127;
+        const int half = mt >> 7;
+        const bool epilogue = warp < 6;
         const int quad = warp & 3;
+        const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
@@ -162,45 +171,49 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (T != 0u || p.mask_bits != nullptr) {
-                const uint32_t xs = smem_u32(smem + s * kStageBytes);
-#pragma unroll 2
-                for (int i = 0; i < 8; ++i) {
-                    const int ch = et + 128 * i;
-                    const int row = ch >> 3;
-                    const int c16 = ch & 7;
-                    const uint32_t addr = xs + row * 128 + ((c16 ^ (row & 7)) << 4);
-                    const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
-                    const int64_t j0 = static_cast<int64_t>(kb) * 64 + c16 * 8;
-                    const uint4 wv = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(j0 >> 3), p.seed_lo,
-                                               p.seed_hi);
-                    if (T != 0u) {
+                const uint32_t xrow = smem_u32(smem + s * kStageBytes) + row * 128;
+                const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
+                uint4 wv[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    wv[i] = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(kb * 8 + half * 4 + i), keys);
+                if (T != 0u) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int c16 = half * 4 + i;
+                        const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
                         uint4 v = lds128(addr);
-                        v.x &= keep_pair_mask(wv.x, T);
-                        v.y &= keep_pair_mask(wv.y, T);
-                        v.z &= keep_pair_mask(wv.z, T);
-                        v.w &= keep_pair_mask(wv.w, T);
+                        v.x = apply_keep(v.x, wv[i].x, T);
+                        v.y = apply_keep(v.y, wv[i].y, T);
+                        v.z = apply_keep(v.z, wv[i].z, T);
+                        v.w = apply_keep(v.w, wv[i].w, T);
                         sts128(addr, v);
                     }
-                    if (p.mask_bits != nullptr && t < p.m && j0 < p.k)
-                        p.mask_bits[t * (p.k >> 3) + (j0 >> 3)] = static_cast<uint8_t>(keep_byte(wv, T));
+                }
+                if (p.mask_bits != nullptr && t < p.m) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t g = static_cast<int64_t>(kb) * 8 + half * 4 + i;
+                        if (g * 8 < p.k) p.mask_bits[t * (p.k >> 3) + g] = static_cast<uint8_t>(keep_byte(wv[i], T));
+                    }
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&masked[s]);
-            if (last) {
+            if (last && epilogue) {
                 const uint32_t b = use & 1u;
                 ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
                 const AdapterDev ad = p.rt.ad[a];
-                const int64_t row = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
+                const int64_t orow = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * static_cast<uint32_t>(rpad_max);
                 for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_ld_wait();
-                    if (row < p.m) {
-                        float* dst = p.S_acc + row * p.ld + c0;
+                    if (orow < p.m) {
+                        float* dst = p.S_acc + orow * p.ld + c0;
 #pragma unroll
                         for (int q = 0; q < 16; q += 4)
                             if (c0 + q < ad.rank)
@@ -210,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
-                ++use;
             }
+            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }

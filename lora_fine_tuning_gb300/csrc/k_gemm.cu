@@ -196,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
     } else {
         const int quad = warp & 3;
+        const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         uint32_t use = 0;
         for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
             const TileCoord tc = tile_coord(tile, p);
@@ -225,8 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
                     for (int g = 0; g < 4; ++g) {
                         const int64_t col0 = static_cast<int64_t>(n0) + c * 32 + g * 8;
-                        const uint4 wv = philox_10(static_cast<uint32_t>(row), static_cast<uint32_t>(col0 >> 3), p.seed_lo,
-                                                   p.seed_hi);
+                        const uint4 wv = philox_10(static_cast<uint32_t>(row), static_cast<uint32_t>(col0 >> 3), keys);
                         const uint32_t keep = keep_byte(wv, T);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)

@@ -99,12 +99,14 @@ def test_empty_batch():
 
 
 def test_repeat_calls_are_deterministic_in_mask_and_close_in_values():
-    m, k, n, r = 384, 512, 512, 16
+    """Masks are bit-identical across calls; S', dA, dB are reduced across CTAs with fp32
+    atomics, so values (and Y, dX through S', dSq) agree up to rounding order."""
+    m, k, n, r = 384, 4096, 512, 16
     raw, out1 = run_single(m, k, n, r, 2.0, 0.1, 21)
     raw, out2 = run_single(m, k, n, r, 2.0, 0.1, 21)
     assert torch.equal(out1["mask"], out2["mask"])
-    assert torch.equal(out1["Y"], out2["Y"])      # the forward GEMM has a fixed reduction order
-    assert torch.equal(out1["dX"], out2["dX"])
+    for name in ("Y", "S", "dX", "dA", "dB"):
+        assert_close(name, host_f64(out1[name]), host_f64(out2[name]), 1e-3)
 
 
 # ---------------------------------------------------------------------------
@@ -191,7 +193,10 @@ def test_multi_with_one_adapter_equals_single():
     dX2 = api.multi_lora_bwd(dY, X, W, ad, [(0, m, 0)], seed, S2)
     torch.cuda.synchronize()
     assert torch.equal(M1, M2)
-    assert torch.equal(Y1, Y2) and torch.equal(S1, S2) and torch.equal(dX1, dX2)
+    # same kernels and routing; values agree up to the order of the fp32 split-K reductions
+    assert_close("Y", host_f64(Y2), host_f64(Y1), 1e-3)
+    assert_close("S", host_f64(S2), host_f64(S1), 1e-3)
+    assert_close("dX", host_f64(dX2), host_f64(dX1), 1e-3)
     assert_close("dA", host_f64(ad[0].dA), host_f64(dA1), 1e-3)
     assert_close("dB", host_f64(ad[0].dB), host_f64(dB1), 1e-3)
 
