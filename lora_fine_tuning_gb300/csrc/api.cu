@@ -96,7 +96,8 @@ lora_status device_setup(int* sms_out) {
             d.status = LORA_EARCH;
         } else {
             d.sms = sms;
-            if (!cuda_ok(down_configure()) || !cuda_ok(gemm_configure()) || !cuda_ok(dsdb_configure()) ||
+            if (!cuda_ok(down_configure()) || !cuda_ok(gemm2_configure()) ||
+                !cuda_ok(dsdb_configure()) ||
                 !cuda_ok(da_configure()))
                 d.status = LORA_ECUDA;
         }
@@ -362,14 +363,10 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     g.M = m;
     g.N = n;
     g.K = k;
-    g.n_mtiles = static_cast<int32_t>((m + 127) / 128);
-    g.n_ntiles = static_cast<int32_t>((n + 255) / 256);
     g.nkb = static_cast<int32_t>((k + 63) / 64);
-    g.group_m = 16;
     g.seed_lo = seed_lo;
     g.seed_hi = seed_hi;
-    const int tiles = g.n_mtiles * g.n_ntiles;
-    LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm_fwd(g, std::min(tiles, c.sms), c.stream); }));
+    LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm2(g, false, 256, c.sms, c.stream); }));
     return LORA_OK;
 }
 
@@ -427,11 +424,12 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         static GemmParams g;
         std::memset(&g, 0, sizeof(g));
         if (!make_map(&g.mapA, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-        if (!make_map(&g.mapB, W, n, k, n, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        if (!make_map(&g.mapB, W, n, k, n, 64, kBwdPairBN / 2, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         if (nad > 0) {
             if (!make_map(&g.mapTA, dsq, c.s_ld, m, c.s_ld, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
             for (int a = 0; a < nad; ++a)
-                if (!make_map(&g.mapTB[a], ads[a].A, ads[a].rank, k, ads[a].rank, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B))
+                if (!make_map(&g.mapTB[a], ads[a].A, ads[a].rank, k, ads[a].rank, 64, kBwdPairBN / 2,
+                              CU_TENSOR_MAP_SWIZZLE_128B))
                     return LORA_ECUDA;
         }
         g.rt = c.rt;
@@ -440,14 +438,10 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         g.M = m;
         g.N = k;
         g.K = n;
-        g.n_mtiles = static_cast<int32_t>((m + 127) / 128);
-        g.n_ntiles = static_cast<int32_t>((k + 255) / 256);
         g.nkb = static_cast<int32_t>((n + 63) / 64);
-        g.group_m = 16;
         g.seed_lo = seed_lo;
         g.seed_hi = seed_hi;
-        const int tiles = g.n_mtiles * g.n_ntiles;
-        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm_bwd(g, std::min(tiles, c.sms), c.stream); }));
+        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, kBwdPairBN, c.sms, c.stream); }));
     }
 
     if (nad > 0) {

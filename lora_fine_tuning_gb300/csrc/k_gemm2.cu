@@ -1,0 +1,355 @@
+// The layer's two dense contractions on CTA pairs (tcgen05 cta_group::2).
+//
+// Products:
+//   forward   Y  = [X | S'] [W ; B_a]                (article section 4.1, ②)
+//   backward  dX = dY W^T + D .* (dSq A_a^T)         (article section 4.1, ⑤)
+// but each output tile is 256 rows x BN columns computed by a cluster of two
+// CTAs: CTA rank r stages rows [256 i + 128 r, +128) of the A operand and
+// half of the B operand's BN columns; the leader (rank 0) issues one
+// tcgen05.mma M=256 that reads both CTAs' shared memory and writes both CTAs'
+// TMEM (each holds its own 128 rows x BN columns).  Per CTA and 64-deep K
+// block that is 16 KB of A and BN/2 x 128 B of B for 128 x BN x 64 MACs,
+// instead of 16 KB + BN x 128 B for a single CTA: fewer bytes in flight
+// per FLOP, so the same shared memory holds a deeper stage ring (6 stages
+// of 32 KB) and covers more load latency.
+//
+// The rank-r branch stays a K-tail of the same loop.  The two 128-row halves
+// of a tile may belong to different adapters; each distinct adapter then gets
+// its own tail pass, in which the rows of the other half load zeros (a TMA box
+// placed wholly outside the tensor).
+//
+// Roles per CTA: warp 0 TMA producer (both CTAs; the leader also posts the
+// expected bytes of both halves on its barrier), warp 1 MMA issue (leader
+// only) and TMEM allocation, warps 2-5 epilogue (both CTAs, own rows).
+#include "cluster.cuh"
+#include "kernels.h"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kGroupPairs = 8;   // rasterisation: pair-rows per group
+
+template <bool kBwd, int BN>
+struct Cfg {
+    static constexpr int BNH = BN / 2;                        // B columns (fwd) / rows (bwd) per CTA
+    static constexpr uint32_t kA = 128u * 128u;                // 128 rows x 64 bf16
+    static constexpr uint32_t kB = static_cast<uint32_t>(BNH) * 128u;
+    static constexpr uint32_t kStage = kA + kB;
+    static constexpr int kStages = (192 * 1024) / kStage > 8 ? 8 : (192 * 1024) / kStage;
+    static constexpr bool kDouble = !kBwd || BN <= 128;       // two accumulator buffers fit in TMEM
+    static constexpr uint32_t kBufCols = kBwd ? 2u * BN : static_cast<uint32_t>(BN);
+};
+
+struct PairTile {
+    int mp, np;
+};
+
+struct Tail {
+    int a[2];    // adapter of each pass (-1: none)
+    int nb[2];   // 64-deep blocks of each pass
+    int total;
+    int half_adapter[2];   // adapter of each 128-row half
+};
+
+__device__ __forceinline__ Tail tail_of(int mp, const GemmParams& p) {
+    Tail t;
+    const int t0 = 2 * mp, t1 = 2 * mp + 1;
+    const int a0 = t0 < p.rt.n_tiles ? p.rt.tile_adapter[t0] : -1;
+    const int a1 = t1 < p.rt.n_tiles ? p.rt.tile_adapter[t1] : -1;
+    t.half_adapter[0] = a0;
+    t.half_adapter[1] = a1;
+    t.a[0] = a0 >= 0 ? a0 : a1;
+    t.a[1] = (a0 >= 0 && a1 >= 0 && a1 != a0) ? a1 : -1;
+    for (int i = 0; i < 2; ++i) t.nb[i] = t.a[i] >= 0 ? (p.rt.ad[t.a[i]].rank + 63) / 64 : 0;
+    t.total = t.nb[0] + t.nb[1];
+    return t;
+}
+
+template <int BN>
+__device__ __forceinline__ PairTile pair_tile(int tile, const GemmParams& p) {
+    const int n_mp = static_cast<int>((p.M + 255) / 256);
+    const int n_np = static_cast<int>((p.N + BN - 1) / BN);
+    const int per_group = kGroupPairs * n_np;
+    const int group = tile / per_group;
+    const int first = group * kGroupPairs;
+    const int gm = min(n_mp - first, kGroupPairs);
+    const int in_group = tile - group * per_group;
+    return PairTile{first + in_group % gm, in_group / gm};
+}
+
+template <bool kBwd, int BN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm2_kernel(const __grid_constant__ GemmParams p) {
+    using C = Cfg<kBwd, BN>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStage);
+    uint64_t* full = bars;            // leader's are used: both halves' bytes land here
+    uint64_t* empty = bars + S;       // per CTA: released by the leader's multicast commit
+    uint64_t* acc_full = bars + 2 * S;
+    uint64_t* acc_empty = acc_full + 2;   // leader's: 128 arrivals from each CTA
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], 256);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.mapA);
+        tma_prefetch_desc(&p.mapB);
+    }
+    tc_fence_before();
+    cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, (kBwd ? kKGemmBwd : kKGemmFwd) << 8};
+
+    const int n_mp = static_cast<int>((p.M + 255) / 256);
+    const int n_np = static_cast<int>((p.N + BN - 1) / BN);
+    const int total = n_mp * n_np;
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = pair; tile < total && ok; tile += npairs) {
+                const PairTile pt = pair_tile<BN>(tile, p);
+                const int m0 = pt.mp * 256 + static_cast<int>(rank) * 128;
+                const int n0 = pt.np * BN + static_cast<int>(rank) * C::BNH;
+                const Tail tl = tail_of(pt.mp, p);
+                const int my_adapter = tl.half_adapter[rank];
+                for (int kb = 0; kb < p.nkb + tl.total; ++kb) {
+                    if (!mbar_wait_cl(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                    uint8_t* as = smem + s * C::kStage;
+                    uint8_t* bs = as + C::kA;
+                    if (leader) mbar_arrive_expect_tx(&full[s], 2u * C::kStage);
+                    const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
+                    if (kb < p.nkb) {
+                        tma_load_2d_pair(as, &p.mapA, fb, kb * 64, m0);
+                        if (kBwd) {
+                            tma_load_2d_pair(bs, &p.mapB, fb, kb * 64, n0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < C::BNH / 64; ++j)
+                                tma_load_2d_pair(bs + j * 8192, &p.mapB, fb, n0 + 64 * j, kb * 64);
+                        }
+                    } else {
+                        const int t = kb - p.nkb;
+                        const int pass = t < tl.nb[0] ? 0 : 1;
+                        const int tb = pass == 0 ? t : t - tl.nb[0];
+                        const int a = tl.a[pass];
+                        // rows of the other adapter's half read zeros (box wholly outside the tensor)
+                        tma_load_2d_pair(as, &p.mapTA, fb, tb * 64, my_adapter == a ? m0 : -256);
+                        if (kBwd) {
+                            tma_load_2d_pair(bs, &p.mapTB[a], fb, tb * 64, n0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < C::BNH / 64; ++j)
+                                tma_load_2d_pair(bs + j * 8192, &p.mapTB[a], fb, n0 + 64 * j, tb * 64);
+                        }
+                    }
+                    ++issued;
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+            }
+            if (!ok && leader) {
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_cl_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t use = 0;
+            const uint32_t idesc = make_idesc_bf16(256, BN, false, !kBwd);
+            bool ok = true;
+            for (int tile = pair; tile < total && ok; tile += npairs) {
+                const PairTile pt = pair_tile<BN>(tile, p);
+                const Tail tl = tail_of(pt.mp, p);
+                const uint32_t b = C::kDouble ? (use & 1u) : 0u;
+                const uint32_t empty_parity = C::kDouble ? (((use >> 1) & 1u) ^ 1u) : ((use & 1u) ^ 1u);
+                if (!mbar_wait_cl(&acc_empty[b], empty_parity, w, 2)) break;
+                tc_fence_after();
+                const uint32_t acc1 = tmem + b * C::kBufCols;
+                const uint32_t acc2 = acc1 + BN;
+                for (int kb = 0; kb < p.nkb + tl.total; ++kb) {
+                    if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t as = smem_u32(smem + s * C::kStage);
+                    const uint32_t bs = as + C::kA;
+                    if (kb < p.nkb) {
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t ad = make_smem_desc(as + ks * 32, 16, 1024, kSw128);
+                            const uint64_t bd = kBwd ? make_smem_desc(bs + ks * 32, 16, 1024, kSw128)
+                                                     : make_smem_desc(bs + ks * 2048, 8192, 1024, kSw128);
+                            umma_bf16_pair(acc1, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+                        }
+                    } else {
+                        const int t = kb - p.nkb;
+                        const int pass = t < tl.nb[0] ? 0 : 1;
+                        const int tb = pass == 0 ? t : t - tl.nb[0];
+                        const int left = p.rt.ad[tl.a[pass]].rank - tb * 64;
+                        const int nks = left >= 64 ? 4 : (left + 15) / 16;
+                        for (int ks = 0; ks < nks; ++ks) {
+                            const uint64_t ad = make_smem_desc(as + ks * 32, 16, 1024, kSw128);
+                            if (kBwd) {
+                                const uint64_t bd = make_smem_desc(bs + ks * 32, 16, 1024, kSw128);
+                                umma_bf16_pair(acc2, ad, bd, idesc, (t | ks) != 0 ? 1u : 0u);
+                            } else {
+                                const uint64_t bd = make_smem_desc(bs + ks * 2048, 8192, 1024, kSw128);
+                                umma_bf16_pair(acc1, ad, bd, idesc, 1u);
+                            }
+                        }
+                    }
+                    umma_commit_pair(&empty[s], 3);
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                if (!ok) break;
+                umma_commit_pair(&acc_full[b], 3);
+                ++use;
+            }
+            umma_commit_pair(drain, 1);
+            mbar_wait_cl_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else {
+        const int quad = warp & 3;
+        const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
+        uint32_t use = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            const PairTile pt = pair_tile<BN>(tile, p);
+            const Tail tl = tail_of(pt.mp, p);
+            const int m0 = pt.mp * 256 + static_cast<int>(rank) * 128;
+            const int n0 = pt.np * BN;
+            const int a = tl.half_adapter[rank];
+            const bool branch = kBwd && a >= 0;
+            const uint32_t T = a >= 0 ? p.rt.ad[a].T : 0u;
+            const uint32_t b = C::kDouble ? (use & 1u) : 0u;
+            const uint32_t full_parity = C::kDouble ? ((use >> 1) & 1u) : (use & 1u);
+            const bool ok = mbar_wait_cl(&acc_full[b], full_parity, w, 4);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after();
+            const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
+            const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+            const uint32_t t1 = tmem + lane_off + b * C::kBufCols;
+            const uint32_t t2 = t1 + BN;
+            uint16_t* out_row = p.out + row * p.N;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t1 + c * 32, v);
+                if (branch) {
+                    uint32_t u[32];
+                    tmem_ld32(t2 + c * 32, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const int64_t col0 = static_cast<int64_t>(n0) + c * 32 + g * 8;
+                        const uint4 wv = philox_10(static_cast<uint32_t>(row), static_cast<uint32_t>(col0 >> 3), keys);
+                        const uint32_t keep = keep_byte(wv, T);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            if ((keep >> e) & 1u)
+                                v[g * 8 + e] =
+                                    __float_as_uint(__uint_as_float(v[g * 8 + e]) + __uint_as_float(u[g * 8 + e]));
+                    }
+                } else {
+                    tmem_ld_wait();
+                }
+                if (row < p.M) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int64_t col = static_cast<int64_t>(n0) + c * 32 + q * 8;
+                        if (col < p.N) {
+                            uint4 pk;
+                            pk.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
+                            pk.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
+                            pk.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
+                            pk.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
+                            stg128(out_row + col, pk);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+            ++use;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // the leader's MMAs and both epilogues are finished
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+template <bool kBwd, int BN>
+size_t smem_bytes() {
+    using C = Cfg<kBwd, BN>;
+    return 1024 + C::kStages * C::kStage + (2 * C::kStages + 5) * 8 + 16;
+}
+
+}  // namespace
+
+cudaError_t gemm2_configure() {
+    cudaError_t e = cudaFuncSetAttribute(gemm2_kernel<false, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<false, 256>()));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm2_kernel<true, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<true, 256>()));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm2_kernel<true, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(smem_bytes<true, 128>()));
+}
+
+cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStream_t stream) {
+    const int n_mp = static_cast<int>((p.M + 255) / 256);
+    const int n_np = static_cast<int>((p.N + bn - 1) / bn);
+    int pairs = n_mp * n_np;
+    if (pairs > sms / 2) pairs = sms / 2;
+    if (pairs < 1) pairs = 1;
+    const dim3 grid(2 * pairs);
+    if (!bwd) {
+        gemm2_kernel<false, 256><<<grid, kThreads, smem_bytes<false, 256>(), stream>>>(p);
+    } else if (bn == 128) {
+        gemm2_kernel<true, 128><<<grid, kThreads, smem_bytes<true, 128>(), stream>>>(p);
+    } else {
+        gemm2_kernel<true, 256><<<grid, kThreads, smem_bytes<true, 256>(), stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace lora

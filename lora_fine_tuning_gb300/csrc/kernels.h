@@ -9,7 +9,6 @@
 namespace lora {
 
 constexpr int kDownStages = 6;
-constexpr int kGemmStages = 4;
 // Dynamic shared memory a kernel may request; leaves room for its few bytes
 // of static shared memory under the 227 KB per-block limit.
 constexpr int kMaxDynSmem = 225 * 1024;
@@ -22,10 +21,11 @@ cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_finalize_s(const float* acc, uint16_t* out, int64_t m, int32_t ld, const Routing& rt, int sms,
                               cudaStream_t stream);
 
-size_t gemm_smem_bytes();
-cudaError_t gemm_configure();
-cudaError_t launch_gemm_fwd(const GemmParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_gemm_bwd(const GemmParams& p, int grid, cudaStream_t stream);
+// CTA-pair GEMM (cta_group::2): forward 256 x 256 tiles (two accumulator
+// buffers); backward 256 x kBwdPairBN (acc1 + acc2 fill TMEM: one buffer).
+constexpr int kBwdPairBN = 256;
+cudaError_t gemm2_configure();
+cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStream_t stream);
 
 size_t dsdb_smem_bytes(const DsDbParams& p);
 cudaError_t dsdb_configure();

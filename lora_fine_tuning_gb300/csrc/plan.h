@@ -66,20 +66,20 @@ struct DownParams {
     int32_t stages;
 };
 
-// GEMM with the rank-r tail.
+// CTA-pair GEMM with the rank-r tail (k_gemm2.cu).
 //  forward:  Y = [X | S'] [W ; B_a]           (B operand MN-major)
 //  backward: dX = dY W^T + D .* (dSq A_a^T)   (B operand K-major; second accumulator)
+// Each CTA of a pair stages half of the B tile, so B boxes are BN/2 wide.
 struct GemmParams {
     CUtensorMap mapA;                  // fwd: X {k, m}; bwd: dY {n, m}; box {64, 128}
-    CUtensorMap mapB;                  // fwd: W {n, k} box {64, 64}; bwd: W {n, k} box {64, 256}
+    CUtensorMap mapB;                  // fwd: W {n, k} box {64, 64}; bwd: W {n, k} box {64, BN/2}
     CUtensorMap mapTA;                 // tail A: fwd S' / bwd dSq, {s_ld, m}, box {64, 128}
-    CUtensorMap mapTB[kMaxAdapters];   // tail B: fwd B_i {n, r_i} box {64, 64}; bwd A_i {r_i, k} box {64, 256}
+    CUtensorMap mapTB[kMaxAdapters];   // tail B: fwd B_i {n, r_i} box {64, 64}; bwd A_i {r_i, k} box {64, BN/2}
     Routing rt;
     DevCtl ctl;
     uint16_t* out;                     // Y (m x n) or dX (m x k), bf16
     int64_t M, N, K;                   // GEMM sizes: fwd (m, n, k), bwd (m, k, n)
-    int32_t n_mtiles, n_ntiles, nkb;
-    int32_t group_m;                   // rasterisation: m-tiles per group
+    int32_t nkb;                       // 64-deep K blocks of the main product
     uint32_t seed_lo, seed_hi;
 };
 

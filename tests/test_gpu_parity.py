@@ -106,7 +106,7 @@ def test_repeat_calls_are_deterministic_in_mask_and_close_in_values():
     raw, out2 = run_single(m, k, n, r, 2.0, 0.1, 21)
     assert torch.equal(out1["mask"], out2["mask"])
     for name in ("Y", "S", "dX", "dA", "dB"):
-        assert_close(name, host_f64(out1[name]), host_f64(out2[name]), 1e-3)
+        assert_close(name, host_f64(out1[name]), host_f64(out2[name]), TOL)
 
 
 # ---------------------------------------------------------------------------
@@ -197,8 +197,9 @@ def test_multi_with_one_adapter_equals_single():
     assert_close("Y", host_f64(Y2), host_f64(Y1), 1e-3)
     assert_close("S", host_f64(S2), host_f64(S1), 1e-3)
     assert_close("dX", host_f64(dX2), host_f64(dX1), 1e-3)
-    assert_close("dA", host_f64(ad[0].dA), host_f64(dA1), 1e-3)
-    assert_close("dB", host_f64(ad[0].dB), host_f64(dB1), 1e-3)
+    # dA, dB pass through dSq (bf16, reduced with atomics): agreement within the parity tolerance
+    assert_close("dA", host_f64(ad[0].dA), host_f64(dA1), TOL)
+    assert_close("dB", host_f64(ad[0].dB), host_f64(dB1), TOL)
 
 
 def test_no_segments_is_frozen_layer():
