@@ -361,17 +361,23 @@ def run_native(args):
             torch.matmul(dY, W.t(), out=dX)
 
         res = {}
+        frozen_kernels = {}
         for label, fn in (("ours", frozen_ours), ("torch_matmul", frozen_torch)):
             fn()
             torch.cuda.synchronize(dev)
+            if label == "ours":
+                native.timing_begin()
             g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             g0.record(stream)
             for _ in range(reps):
                 fn()
             g1.record(stream)
             torch.cuda.synchronize(dev)
+            if label == "ours":
+                frozen_kernels = {kname: ms / max(1, cnt) for kname, (ms, cnt) in native.timing_end().items()}
             res[label] = max_over_ranks(g0.elapsed_time(g1)) / reps
         frozen = {"frozen_ms_per_step_ours": res["ours"], "frozen_ms_per_step_torch": res["torch_matmul"],
+                  "frozen_ms_per_launch_ours": frozen_kernels,
                   "lora_overhead_vs_ours": ms_per_step / res["ours"],
                   "lora_overhead_vs_torch": ms_per_step / res["torch_matmul"]}
 

@@ -41,8 +41,10 @@
  *    pointer 16-byte aligned, 0 <= p < 1, m <= 262144 rows.
  *  - Gradients dA, dB are overwritten, not accumulated.
  *  - `workspace` is device memory of at least lora_workspace_size() bytes,
- *    256-byte aligned.  One workspace must not be used by two calls that may
- *    run concurrently.
+ *    256-byte aligned, filled with zeros before its first use (cudaMemset).
+ *    Every call that completes leaves it zeroed again; after a call reports
+ *    LORA_EDEVICE_TIMEOUT, zero it before reusing it.  One workspace must not
+ *    be used by two calls that may run concurrently.
  */
 #ifndef LORA_GB300_H
 #define LORA_GB300_H
@@ -120,7 +122,7 @@ lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
 /* Forward, packed multi-adapter batch.  `adapters` and `segments` are HOST
  * arrays, read before the call returns.  S_saved is m x s_ld with
  * s_ld = the largest adapter rank; row t of adapter i holds alpha_i S in
- * columns [0, r_i) and zeros after; rows without an adapter are zero.
+ * columns [0, r_i) and zeros after; rows without an adapter are not written.
  * mask_bits (optional) is written for rows that have an adapter.
  * n_adapters may be 0 only with n_segments == 0 (the frozen layer alone). */
 lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters, int32_t n_adapters,
@@ -152,10 +154,13 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
  *    clears its status word, on `stream`; make that first call before any
  *    stream capture.
  *  - Every call on a device shares the one array and leaves its contents
- *    behind; each call clears what it needs at zero.  Calls whose work can
- *    overlap on the GPU (different streams, no ordering) race on the array.
+ *    behind.  The first call on a device clears the whole array; every call
+ *    that completes leaves its accumulators and counters at zero again, so
+ *    the next call starts clean.  Calls whose work can overlap on the GPU
+ *    (different streams, no ordering) race on the array.
  *  - Bounded-wait timeouts are recorded in the array's status word, which no
- *    entry point reads back. */
+ *    entry point reads back; a call that timed out may leave the array dirty,
+ *    and later results on that device are then not to be trusted. */
 enum { LORA_STATIC_SCRATCH_BYTES = 8 << 20 };
 lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
                                     float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r,
@@ -191,8 +196,8 @@ const char* lora_status_string(lora_status s);
  * fills, for each kind i < n_kinds (see lora_kernel_name), the summed device
  * time in ms and the number of launches.  Kinds: 0 down-projection,
  * 1 finalize S, 2 forward GEMM, 3 dS/dB, 4 finalize dS/dB, 5 backward GEMM,
- * 6 dA, 7 finalize dA, 8 workspace memset.  Host-side cost: two event
- * records per launch. */
+ * 6 dA, 7 finalize dA, 8 memset (gradients of adapters that own no rows).
+ * Host-side cost: two event records per launch. */
 enum { LORA_KERNEL_KINDS = 9 };
 lora_status lora_timing_begin(void);
 lora_status lora_timing_end(float* total_ms, int32_t* launches, int32_t n_kinds);

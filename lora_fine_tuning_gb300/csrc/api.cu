@@ -42,10 +42,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // optional per-kernel timing (measurement tools): events around each launch
 // ---------------------------------------------------------------------------
 
-enum Kind : int {
-    kDownProj = 0, kFinalizeS, kGemmFwd, kDsDb, kFinalizeBwd1, kGemmBwd, kDa, kFinalizeDa, kMemset, kKinds
-};
-const char* const kKindNames[kKinds] = {"down_proj", "finalize_s", "gemm_fwd", "ds_db", "finalize_bwd1",
+enum Kind : int { kDownProj = 0, kFinalizeS, kGemmFwd, kDsDb, kFinalize, kGemmBwd, kDa, kFinalizeDa, kMemset, kKinds };
+const char* const kKindNames[kKinds] = {"down_proj", "finalize_s", "gemm_fwd", "ds_db", "finalize_ds_db",
                                         "gemm_bwd", "da", "finalize_da", "memset"};
 
 struct TimingRec {
@@ -202,6 +200,8 @@ lora_status tile_table(const lora_segment* seg, int32_t nseg, int32_t nad, int64
 constexpr size_t kAlign = 256;
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
+// Every byte below is zero between calls: each finalize kernel clears the
+// accumulators it reads, and finalize_da (after dSq's last reader) clears dSq.
 struct Layout {
     size_t status = 0;      // int32 device status word
     size_t s_acc = 0;       // m x s_ld fp32 (forward S, backward dS)
@@ -315,36 +315,33 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     if (m == 0) return LORA_OK;
     const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
     const int nad = c.rt.n_adapters;
-    float* s_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
 
-    if (nad > 0) {
-        LORA_CUDA(timed(kMemset, c.stream, [&] { return cudaMemsetAsync(s_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream); }));
-        if (c.rt.n_active > 0) {
-            static DownParams p;  // large: keep it off the stack
-            std::memset(&p, 0, sizeof(p));
-            if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-            for (int a = 0; a < nad; ++a) {
-                const int rp = c.rpads[a];
-                if (!make_map(&p.mapA[a], ads[a].A, ads[a].rank, k, ads[a].rank, std::min(rp, 64), 64,
-                              rank_swizzle_host(rp)))
-                    return LORA_ECUDA;
-            }
-            p.rt = c.rt;
-            p.ctl = ctl_of(c);
-            p.S_acc = s_acc;
-            p.mask_bits = mask_bits;
-            p.m = m;
-            p.k = k;
-            p.ld = c.s_ld;
-            p.nkb = static_cast<int32_t>((k + 63) / 64);
-            p.units = static_cast<int64_t>(c.rt.n_active) * p.nkb;
-            p.seed_lo = seed_lo;
-            p.seed_hi = seed_hi;
-            p.stages = kDownStages;
-            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
+    if (nad > 0 && c.rt.n_active > 0) {
+        static DownParams p;  // large: keep it off the stack
+        std::memset(&p, 0, sizeof(p));
+        if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        for (int a = 0; a < nad; ++a) {
+            const int rp = c.rpads[a];
+            if (!make_map(&p.mapA[a], ads[a].A, ads[a].rank, k, ads[a].rank, std::min(rp, 64), 64,
+                          rank_swizzle_host(rp)))
+                return LORA_ECUDA;
         }
-        LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(s_acc, S_saved, m, c.s_ld, c.rt, c.sms, c.stream); }));
+        p.rt = c.rt;
+        p.ctl = ctl_of(c);
+        p.S_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
+        p.S_out = S_saved;
+        p.mask_bits = mask_bits;
+        p.m = m;
+        p.k = k;
+        p.ld = c.s_ld;
+        p.nkb = static_cast<int32_t>((k + 63) / 64);
+        p.units = static_cast<int64_t>(c.rt.n_active) * p.nkb;
+        p.seed_lo = seed_lo;
+        p.seed_hi = seed_hi;
+        p.stages = kDownStages;
+        const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
+        LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));
     }
 
     static GemmParams g;
@@ -374,50 +371,50 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
                     uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, uint16_t* dX) {
     const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
     const int nad = c.rt.n_adapters;
-    float* ds_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
     uint16_t* dsq = reinterpret_cast<uint16_t*>(c.ws + c.L.dsq);
     float* acc = reinterpret_cast<float*>(c.ws + c.L.acc);
-    AdapterPtrs dBp{}, dAp{};
+
+    // Adapters that own no rows get zero gradients (no kernel finishes them).
     for (int a = 0; a < nad; ++a) {
-        dBp.p[a] = ads[a].dB;
-        dAp.p[a] = ads[a].dA;
+        if (c.rt.adapter_begin[a + 1] > c.rt.adapter_begin[a]) continue;
+        LORA_CUDA(timed(kMemset, c.stream, [&] {
+            return cudaMemsetAsync(ads[a].dA, 0, static_cast<size_t>(k) * ads[a].rank * 2, c.stream);
+        }));
+        LORA_CUDA(timed(kMemset, c.stream, [&] {
+            return cudaMemsetAsync(ads[a].dB, 0, static_cast<size_t>(n) * ads[a].rank * 2, c.stream);
+        }));
     }
 
-    if (nad > 0) {
-        if (m > 0)
-            LORA_CUDA(timed(kMemset, c.stream,
-                            [&] { return cudaMemsetAsync(ds_acc, 0, static_cast<size_t>(m) * c.s_ld * 4, c.stream); }));
-        LORA_CUDA(timed(kMemset, c.stream, [&] { return cudaMemsetAsync(acc, 0, c.L.acc_floats * 4, c.stream); }));
-        if (c.rt.n_active > 0) {
-            static DsDbParams p;
-            std::memset(&p, 0, sizeof(p));
-            if (!make_map(&p.mapDY, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-            for (int a = 0; a < nad; ++a) {
-                const int rp = c.rpads[a];
-                if (!make_map(&p.mapB[a], ads[a].B, n, ads[a].rank, n, 64, rp, CU_TENSOR_MAP_SWIZZLE_128B))
-                    return LORA_ECUDA;
-                if (!make_map(&p.mapS[a], S_saved, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
-                    return LORA_ECUDA;
-            }
-            p.rt = c.rt;
-            p.ctl = ctl_of(c);
-            p.dS_acc = ds_acc;
-            p.acc_base = acc;
-            p.m = m;
-            p.n = n;
-            p.ld = c.s_ld;
-            p.nnb = static_cast<int32_t>((n + 127) / 128);
-            p.units = static_cast<int64_t>(c.rt.n_active) * p.nnb;
-            const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
-            p.off_b = 32768;
-            p.off_s = p.off_b + 2 * 128 * rpm;
-            p.stage_bytes = p.off_s + 256 * rpm;
-            p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
-            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
+    if (nad > 0 && c.rt.n_active > 0) {
+        static DsDbParams p;
+        std::memset(&p, 0, sizeof(p));
+        if (!make_map(&p.mapDY, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        for (int a = 0; a < nad; ++a) {
+            const int rp = c.rpads[a];
+            if (!make_map(&p.mapB[a], ads[a].B, n, ads[a].rank, n, 64, rp, CU_TENSOR_MAP_SWIZZLE_128B))
+                return LORA_ECUDA;
+            if (!make_map(&p.mapS[a], S_saved, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
+                return LORA_ECUDA;
+            p.dB.p[a] = ads[a].dB;
         }
-        LORA_CUDA(timed(kFinalizeBwd1, c.stream,
-                        [&] { return launch_finalize_bwd1(ds_acc, dsq, m, c.s_ld, acc, dBp, n, c.rt, c.sms, c.stream); }));
+        p.rt = c.rt;
+        p.ctl = ctl_of(c);
+        p.dS_acc = reinterpret_cast<float*>(c.ws + c.L.s_acc);
+        p.acc_base = acc;
+        p.dSq = dsq;
+        p.m = m;
+        p.n = n;
+        p.ld = c.s_ld;
+        p.nnb = static_cast<int32_t>((n + 127) / 128);
+        p.units = static_cast<int64_t>(c.rt.n_active) * p.nnb;
+        const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
+        p.off_b = 32768;
+        p.off_s = p.off_b + 2 * 128 * rpm;
+        p.stage_bytes = p.off_s + 256 * rpm;
+        p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
+        const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
+        LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, c.sms, c.stream); }));
     }
 
     if (m > 0) {
@@ -444,39 +441,40 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, kBwdPairBN, c.sms, c.stream); }));
     }
 
-    if (nad > 0) {
-        if (c.rt.n_active > 0) {
-            static DaParams p;
-            std::memset(&p, 0, sizeof(p));
-            if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-            for (int a = 0; a < nad; ++a) {
-                const int rp = c.rpads[a];
-                if (!make_map(&p.mapD[a], dsq, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
-                    return LORA_ECUDA;
-            }
-            p.rt = c.rt;
-            p.ctl = ctl_of(c);
-            p.acc_base = acc;
-            p.m = m;
-            p.k = k;
-            p.nfb = static_cast<int32_t>((k + 127) / 128);
-            int64_t u = 0;
-            for (int a = 0; a <= nad; ++a) {
-                p.unit_begin[a] = u;
-                if (a < nad) u += static_cast<int64_t>(p.nfb) * (c.rt.adapter_begin[a + 1] - c.rt.adapter_begin[a]);
-            }
-            for (int a = nad + 1; a <= kMaxAdapters; ++a) p.unit_begin[a] = u;
-            p.units = u;
-            p.seed_lo = seed_lo;
-            p.seed_hi = seed_hi;
-            const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
-            p.off_d = 32768;
-            p.stage_bytes = p.off_d + 256 * rpm;
-            p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
-            const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-            LORA_CUDA(timed(kDa, c.stream, [&] { return launch_da(p, grid, c.stream); }));
+    if (nad > 0 && c.rt.n_active > 0) {
+        static DaParams p;
+        std::memset(&p, 0, sizeof(p));
+        if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        for (int a = 0; a < nad; ++a) {
+            const int rp = c.rpads[a];
+            if (!make_map(&p.mapD[a], dsq, c.s_ld, m, c.s_ld, std::min(rp, 64), 128, rank_swizzle_host(rp)))
+                return LORA_ECUDA;
+            p.dA.p[a] = ads[a].dA;
         }
-        LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(acc, dAp, k, c.rt, c.sms, c.stream); }));
+        p.rt = c.rt;
+        p.ctl = ctl_of(c);
+        p.acc_base = acc;
+        p.dsq = dsq;
+        p.ld = c.s_ld;
+        p.m = m;
+        p.k = k;
+        p.nfb = static_cast<int32_t>((k + 127) / 128);
+        int64_t u = 0;
+        for (int a = 0; a <= nad; ++a) {
+            p.unit_begin[a] = u;
+            if (a < nad) u += static_cast<int64_t>(p.nfb) * (c.rt.adapter_begin[a + 1] - c.rt.adapter_begin[a]);
+        }
+        for (int a = nad + 1; a <= kMaxAdapters; ++a) p.unit_begin[a] = u;
+        p.units = u;
+        p.seed_lo = seed_lo;
+        p.seed_hi = seed_hi;
+        const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
+        p.off_d = 32768;
+        p.stage_bytes = p.off_d + 256 * rpm;
+        p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
+        const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        LORA_CUDA(timed(kDa, c.stream, [&] { return launch_da(p, grid, c.stream); }));
+        LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(p, c.sms, c.stream); }));
     }
     return LORA_OK;
 }
@@ -574,8 +572,9 @@ lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, cons
             // array is only a stand-in, so look up its device address.
             void* ptr = nullptr;
             if (!cuda_ok(cudaGetSymbolAddress(&ptr, g_static_scratch))) return LORA_ECUDA;
-            // The device status word must start at zero.
-            if (!cuda_ok(cudaMemsetAsync(ptr, 0, kAlign, static_cast<cudaStream_t>(stream)))) return LORA_ECUDA;
+            // The status word, accumulators and counters must start at zero.
+            if (!cuda_ok(cudaMemsetAsync(ptr, 0, kStaticScratchBytes, static_cast<cudaStream_t>(stream))))
+                return LORA_ECUDA;
             g_static_scratch_ptr[dev] = ptr;
         }
         scratch = g_static_scratch_ptr[dev];

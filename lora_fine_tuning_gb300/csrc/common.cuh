@@ -336,6 +336,42 @@ __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
 }
 
 // ---------------------------------------------------------------------------
+// finishing fp32 accumulators
+// ---------------------------------------------------------------------------
+
+// Four fp32 accumulators read from L2 (written there by reductions).
+__device__ __forceinline__ float4 ld_l2_f4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+__device__ __forceinline__ void st_zero_f4(float* p) {
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+__device__ __forceinline__ uint16_t bf16_bits(float v) { return static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
+
+// Row of an fp32 accumulator -> bf16 row: out[c] = scale * acc[c] for c < valid,
+// 0 for valid <= c < width; the accumulator row is zeroed.  width % 8 == 0.
+__device__ __forceinline__ void finish_row(float* acc, uint16_t* out, int valid, int width, float scale) {
+    for (int c0 = 0; c0 < width; c0 += 8) {
+        float v[8];
+        if (c0 < valid) {
+            const float4 a = ld_l2_f4(acc + c0);
+            const float4 b = ld_l2_f4(acc + c0 + 4);
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            st_zero_f4(acc + c0);
+            st_zero_f4(acc + c0 + 4);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * scale : 0.f;
+        uint4 pk;
+        pk.x = pack_bf16x2(v[0], v[1]);
+        pk.y = pack_bf16x2(v[2], v[3]);
+        pk.z = pack_bf16x2(v[4], v[5]);
+        pk.w = pack_bf16x2(v[6], v[7]);
+        stg128(out + c0, pk);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // CTA prologue / epilogue helpers shared by the warp-specialised kernels
 // ---------------------------------------------------------------------------
 

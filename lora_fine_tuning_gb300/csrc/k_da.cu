@@ -10,6 +10,8 @@
 // MN-major (M = 128 features, N = rank, K = 128 tokens) accumulating over a
 // CTA's run of tiles of one (adapter, feature block), and the run's partial is
 // added into the adapter's fp32 accumulator with vector reductions.
+// finalize_da then writes dA in bf16 and clears the accumulators and dSq
+// (dA is dSq's last reader), so the workspace ends the call all zeros.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -223,21 +225,28 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     }
 }
 
-// dA_a[j, c] = bf16(acc_a[j, c]) for c < r_a.
-__global__ void finalize_da_kernel(const float* __restrict__ acc_base, int64_t k, const __grid_constant__ Routing rt,
-                                   const __grid_constant__ AdapterPtrs dap) {
+// dA_a = bf16(acc_a) (k x r_a), accumulators cleared; dSq rows of active tiles cleared.
+__global__ void finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
+                                   int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     for (int a = 0; a < rt.n_adapters; ++a) {
         const AdapterDev ad = rt.ad[a];
-        const int64_t total = k * ad.rank;
-        const float* src = acc_base + ad.dA_off;
-        uint16_t* dst = dap.p[a];
+        if (rt.adapter_begin[a + 1] == rt.adapter_begin[a]) continue;
+        const int g8 = ad.rank / 8;
+        const int64_t total = k * g8;
         for (int64_t i = tid; i < total; i += stride) {
-            const int64_t j = i / ad.rank;
-            const int64_t c = i - j * ad.rank;
-            dst[i] = static_cast<uint16_t>(pack_bf16x2(src[j * ad.rpad + c], 0.f) & 0xFFFFu);
+            const int64_t j = i / g8;
+            const int c0 = static_cast<int>(i - j * g8) * 8;
+            finish_row(acc_base + ad.dA_off + j * ad.rpad + c0, dap.p[a] + j * ad.rank + c0, 8, 8, 1.0f);
         }
+    }
+    const int g8 = ld / 8;
+    const int64_t total = m * g8;
+    for (int64_t i = tid; i < total; i += stride) {
+        const int64_t t = i / g8;
+        if (rt.tile_adapter[t >> 7] < 0) continue;
+        stg128(dsq + t * ld + (i - t * g8) * 8, make_uint4(0u, 0u, 0u, 0u));
     }
 }
 
@@ -269,9 +278,8 @@ cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_da(const float* acc_base, const AdapterPtrs& dA, int64_t k, const Routing& rt, int sms,
-                               cudaStream_t stream) {
-    finalize_da_kernel<<<4 * sms, 256, 0, stream>>>(acc_base, k, rt, dA);
+cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream) {
+    finalize_da_kernel<<<2 * sms, 256, 0, stream>>>(p.acc_base, p.k, p.dsq, p.m, p.ld, p.rt, p.dA);
     return cudaGetLastError();
 }
 

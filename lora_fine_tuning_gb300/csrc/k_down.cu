@@ -14,7 +14,8 @@
 //  - at the end of each tile range, warps 2..5 read TMEM and add the fp32
 //    partial into S_acc with vector reductions (ranges of one tile may be
 //    split over CTAs: units are spread evenly, stream-K style).
-// The scale alpha/(1-p) and the bf16 rounding are applied by finalize_s.
+// finalize_s then applies alpha/(1-p), writes S' in bf16 and clears S_acc,
+// which starts every call at zero.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -237,17 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     }
 }
 
-__global__ void finalize_s_kernel(const float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
+// S'[t, c] = bf16(alpha_a / (1 - p_a) * S_acc[t, c]) for c < r_a, 0 for
+// r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.
+__global__ void finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
                                   const __grid_constant__ Routing rt) {
-    const int64_t total = m * ld;
+    const int g8 = ld / 8;
+    const int64_t total = m * g8;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = i / ld;
-        const int c = static_cast<int>(i - t * ld);
+        const int64_t t = i / g8;
+        const int c0 = static_cast<int>(i - t * g8) * 8;
         const int a = rt.tile_adapter[t >> 7];
-        float v = 0.f;
-        if (a >= 0 && c < rt.ad[a].rank) v = acc[i] * rt.ad[a].scale;
-        out[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+        if (a < 0) continue;
+        finish_row(acc + t * ld + c0, out + t * ld + c0, rt.ad[a].rank - c0, 8, rt.ad[a].scale);
     }
 }
 
@@ -265,13 +268,8 @@ cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_s(const float* acc, uint16_t* out, int64_t m, int32_t ld, const Routing& rt, int sms,
-                              cudaStream_t stream) {
-    const int64_t total = m * ld;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 4L * sms) blocks = 4L * sms;
-    if (blocks < 1) blocks = 1;
-    finalize_s_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(acc, out, m, ld, rt);
+cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream) {
+    finalize_s_kernel<<<2 * sms, 256, 0, stream>>>(p.S_acc, p.S_out, p.m, p.ld, p.rt);
     return cudaGetLastError();
 }
 

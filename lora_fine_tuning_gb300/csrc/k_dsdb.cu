@@ -11,7 +11,9 @@
 // K = tokens).  dS accumulates in TMEM over a CTA's run of n blocks of one
 // tile; dB^T is produced per unit in a double-buffered accumulator.  Both are
 // flushed with fp32 vector reductions into workspace accumulators (several
-// CTAs share a tile or an n block); finalize_bwd1 scales and rounds them.
+// CTAs share a tile or an n block); finalize_bwd1 then scales and rounds
+// them (dSq = bf16(alpha/(1-p) dS), dB = bf16(dB^T) transposed) and clears
+// the accumulators, which start every call at zero.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
                     }
                 }
+                tc_fence_before();
+                mbar_arrive(&accB_empty[bb]);
             }
-            tc_fence_before();
-            mbar_arrive(&accB_empty[bb]);
             ++units_done;
             if (last) {
                 ok = mbar_wait(accS_full, items_done & 1u, w, 6);
@@ -228,31 +230,58 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
     }
 }
 
-// dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0;
-// dB_a[c, j] = bf16(dB^T_acc_a[j, c]).
-__global__ void finalize_bwd1_kernel(const float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m,
-                                     int32_t ld, const float* __restrict__ acc_base, int64_t n,
-                                     const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dbp) {
+// dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0, on
+// rows of active tiles; dB_a[c, j] = bf16(dB^T_acc_a[j, c]).  Every
+// accumulator read is cleared.
+__global__ void finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
+                                     float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
+                                     const __grid_constant__ AdapterPtrs dbp) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    const int64_t total_s = m * ld;
+    // dS: one thread per 8 columns of a row
+    const int g8 = ld / 8;
+    const int64_t total_s = m * g8;
     for (int64_t i = tid; i < total_s; i += stride) {
-        const int64_t t = i / ld;
-        const int c = static_cast<int>(i - t * ld);
+        const int64_t t = i / g8;
+        const int c0 = static_cast<int>(i - t * g8) * 8;
         const int a = rt.tile_adapter[t >> 7];
-        float v = 0.f;
-        if (a >= 0 && c < rt.ad[a].rank) v = dS_acc[i] * rt.ad[a].scale;
-        dSq[i] = static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu);
+        if (a < 0) continue;
+        const int valid = rt.ad[a].rank;
+        float v[8];
+        if (c0 < valid) {
+            float* src = dS_acc + t * ld + c0;
+            const float4 x = *reinterpret_cast<const float4*>(src);
+            const float4 y = *reinterpret_cast<const float4*>(src + 4);
+            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+            st_zero_f4(src);
+            st_zero_f4(src + 4);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * rt.ad[a].scale : 0.f;
+        uint4 pk;
+        pk.x = pack_bf16x2(v[0], v[1]);
+        pk.y = pack_bf16x2(v[2], v[3]);
+        pk.z = pack_bf16x2(v[4], v[5]);
+        pk.w = pack_bf16x2(v[6], v[7]);
+        stg128(dSq + t * ld + c0, pk);
     }
+    // dB: one thread per (4 ranks, column j); writes are coalesced along j
     for (int a = 0; a < rt.n_adapters; ++a) {
         const AdapterDev ad = rt.ad[a];
-        const int64_t total = static_cast<int64_t>(ad.rank) * n;
-        const float* src = acc_base + ad.dB_off;
+        if (rt.adapter_begin[a + 1] == rt.adapter_begin[a]) continue;
+        const int64_t total = static_cast<int64_t>(ad.rank / 4) * n;
+        float* src = acc_base + ad.dB_off;
         uint16_t* dst = dbp.p[a];
         for (int64_t i = tid; i < total; i += stride) {
-            const int64_t c = i / n;
-            const int64_t j = i - c * n;
-            dst[i] = static_cast<uint16_t>(pack_bf16x2(src[j * ad.rpad + c], 0.f) & 0xFFFFu);
+            const int64_t c4 = i / n;
+            const int64_t j = i - c4 * n;
+            float* q = src + j * ad.rpad + c4 * 4;
+            const float4 x = *reinterpret_cast<const float4*>(q);
+            st_zero_f4(q);
+            dst[(c4 * 4 + 0) * n + j] = bf16_bits(x.x);
+            dst[(c4 * 4 + 1) * n + j] = bf16_bits(x.y);
+            dst[(c4 * 4 + 2) * n + j] = bf16_bits(x.z);
+            dst[(c4 * 4 + 3) * n + j] = bf16_bits(x.w);
         }
     }
 }
@@ -270,9 +299,8 @@ cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_finalize_bwd1(const float* dS_acc, uint16_t* dSq, int64_t m, int32_t ld, const float* acc_base,
-                                 const AdapterPtrs& dB, int64_t n, const Routing& rt, int sms, cudaStream_t stream) {
-    finalize_bwd1_kernel<<<4 * sms, 256, 0, stream>>>(dS_acc, dSq, m, ld, acc_base, n, rt, dB);
+cudaError_t launch_finalize_bwd1(const DsDbParams& p, int sms, cudaStream_t stream) {
+    finalize_bwd1_kernel<<<2 * sms, 256, 0, stream>>>(p.dS_acc, p.dSq, p.m, p.ld, p.acc_base, p.n, p.rt, p.dB);
     return cudaGetLastError();
 }
 

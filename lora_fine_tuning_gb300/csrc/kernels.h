@@ -18,8 +18,7 @@ constexpr int kStageBudget = 220 * 1024;
 size_t down_smem_bytes(int stages);
 cudaError_t down_configure();
 cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_finalize_s(const float* acc, uint16_t* out, int64_t m, int32_t ld, const Routing& rt, int sms,
-                              cudaStream_t stream);
+cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream);
 
 // CTA-pair GEMM (cta_group::2): forward 256 x 256 tiles (two accumulator
 // buffers); backward 256 x kBwdPairBN (acc1 + acc2 fill TMEM: one buffer).
@@ -30,14 +29,12 @@ cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStr
 size_t dsdb_smem_bytes(const DsDbParams& p);
 cudaError_t dsdb_configure();
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_finalize_bwd1(const float* dS_acc, uint16_t* dSq, int64_t m, int32_t ld, const float* acc_base,
-                                 const AdapterPtrs& dB, int64_t n, const Routing& rt, int sms, cudaStream_t stream);
+cudaError_t launch_finalize_bwd1(const DsDbParams& p, int sms, cudaStream_t stream);
 
 size_t da_smem_bytes(const DaParams& p);
 cudaError_t da_configure();
 cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_finalize_da(const float* acc_base, const AdapterPtrs& dA, int64_t k, const Routing& rt, int sms,
-                               cudaStream_t stream);
+cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream);
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream);
 

@@ -56,7 +56,8 @@ struct DownParams {
     CUtensorMap mapA[kMaxAdapters];    // A_i: dims {r_i, k}, box {min(rpad,64), 64}, swizzle by rpad
     Routing rt;
     DevCtl ctl;
-    float* S_acc;                      // m x ld fp32
+    float* S_acc;                      // m x ld fp32 (zero on entry; cleared by finalize_s)
+    uint16_t* S_out;                   // S' = bf16(alpha/(1-p) S), m x ld
     uint8_t* mask_bits;                // optional, m x k/8
     int64_t m, k;
     int32_t ld;                        // s_ld
@@ -92,8 +93,10 @@ struct DsDbParams {
     CUtensorMap mapS[kMaxAdapters];    // S' {s_ld, m}, box {min(rpad,64), 128}, swizzle by rpad (MN-major)
     Routing rt;
     DevCtl ctl;
-    float* dS_acc;                     // m x ld fp32
-    float* acc_base;                   // adapter accumulators (dB_off)
+    float* dS_acc;                     // m x ld fp32 (zero on entry; cleared by finalize_bwd1)
+    float* acc_base;                   // adapter accumulators (dB_off; same)
+    uint16_t* dSq;                     // bf16(alpha/(1-p) dS), m x ld (written by finalize_bwd1)
+    AdapterPtrs dB;                    // per adapter: dB_i (r_i x n)
     int64_t m, n;
     int32_t ld;
     int32_t nnb;                       // ceil(n / 128)
@@ -108,7 +111,10 @@ struct DaParams {
     CUtensorMap mapD[kMaxAdapters];    // dSq {s_ld, m}, box {min(rpad,64), 128}, swizzle by rpad (MN-major)
     Routing rt;
     DevCtl ctl;
-    float* acc_base;                   // adapter accumulators (dA_off)
+    float* acc_base;                   // adapter accumulators (dA_off; zero on entry; cleared by finalize_da)
+    AdapterPtrs dA;                    // per adapter: dA_i (k x r_i)
+    uint16_t* dsq;                     // dSq (m x ld): cleared by finalize_da after its last read
+    int32_t ld;
     int64_t m, k;
     int32_t nfb;                       // ceil(k / 128)
     int64_t units;                     // nfb * n_active

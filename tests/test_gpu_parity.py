@@ -148,7 +148,8 @@ def check_multi(k, n, segments, raw, specs, seed, adapters, Y, S, mask, dX, rows
     for i, ad in enumerate(ads_o):
         sel = np.nonzero(owner == i)[0]
         S_ref[sel, :ad["A"].shape[1]] = ad["alpha"] * S_list[i]
-    assert_close("S_saved", S_host, S_ref)
+    rows = owner >= 0          # rows without an adapter are not written
+    assert_close("S_saved", S_host[rows], S_ref[rows])
     # keep masks bit-exact on rows that have an adapter
     mbits = mask.cpu().numpy()
     for i, ad in enumerate(ads_o):
@@ -230,3 +231,17 @@ def test_stuck_wait_reports_timeout_and_context_survives():
     assert api.lora_device_status(ws) == 0  # cleared by the read
     raw, out = run_single(128, 128, 128, 16, 1.0, 0.1, 5)
     check_single_full(raw, out, 1.0, 0.1, 5)
+
+
+def test_workspace_is_left_zeroed():
+    """Each call leaves the workspace all zeros, so calls of any shape can share it."""
+    m, k, n, r = 640, 1032, 392, 24
+    raw = synth.layer_inputs(51, m, k, n, r)
+    X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
+    ws = torch.zeros(api.lora_workspace_size(m, k, n, r), dtype=torch.uint8, device="cuda")
+    Y, S, _ = api.lora_fwd(X, W, A, B, 1.0, 0.2, 51, ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
+    api.lora_bwd(dY, X, W, A, B, S, 1.0, 0.2, 51, ws=ws)
+    torch.cuda.synchronize()
+    assert int(ws.count_nonzero()) == 0
