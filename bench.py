@@ -350,7 +350,7 @@ def run_native(args):
     # --- frozen-layer reference points (overhead of the LoRA branch) ---
     frozen = None
     if not args.no_frozen:
-        reps = max(3, min(args.steps, 20))
+        reps = args.steps   # same length as the timed LoRA loop, so both see the same clock behaviour
 
         def frozen_ours():
             api.multi_lora_fwd(X, W, [], [], seed, Y=Y, ws=wsb, stream=stream)
