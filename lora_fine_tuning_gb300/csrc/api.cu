@@ -354,6 +354,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
             if (!make_map(&g.mapTB[a], ads[a].B, n, ads[a].rank, n, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
                 return LORA_ECUDA;
     }
+    if (!make_map(&g.mapOut, Y, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
     g.rt = c.rt;
     g.ctl = ctl_of(c);
     g.out = Y;
@@ -429,6 +430,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
                               CU_TENSOR_MAP_SWIZZLE_128B))
                     return LORA_ECUDA;
         }
+        if (!make_map(&g.mapOut, dX, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         g.rt = c.rt;
         g.ctl = ctl_of(c);
         g.out = dX;

@@ -20,7 +20,9 @@
 //
 // Roles per CTA: warp 0 TMA producer (both CTAs; the leader also posts the
 // expected bytes of both halves on its barrier), warp 1 MMA issue (leader
-// only) and TMEM allocation, warps 2-5 epilogue (both CTAs, own rows).
+// only) and TMEM allocation, warps 2-5 epilogue (both CTAs, own rows): the
+// output goes through a swizzled shared-memory block and a TMA tensor store,
+// so global writes are whole 128-byte lines.
 #include "cluster.cuh"
 #include "kernels.h"
 
@@ -39,6 +41,7 @@ struct Cfg {
     static constexpr uint32_t kB = static_cast<uint32_t>(BNH) * 128u;
     static constexpr uint32_t kStage = kA + kB;
     static constexpr int kStages = (192 * 1024) / kStage > 8 ? 8 : (192 * 1024) / kStage;
+    static constexpr uint32_t kStaging = 2u * 16384u;           // two 128 x 64 bf16 output buffers
     static constexpr bool kDouble = !kBwd || BN <= 128;       // two accumulator buffers fit in TMEM
     static constexpr uint32_t kBufCols = kBwd ? 2u * BN : static_cast<uint32_t>(BN);
 };
@@ -87,7 +90,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * C::kStage);
+    uint8_t* staging = smem + S * C::kStage;   // epilogue: output blocks on their way to a TMA store
+    uint64_t* bars = reinterpret_cast<uint64_t*>(staging + C::kStaging);
     uint64_t* full = bars;            // leader's are used: both halves' bytes land here
     uint64_t* empty = bars + S;       // per CTA: released by the leader's multicast commit
     uint64_t* acc_full = bars + 2 * S;
@@ -243,9 +247,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait_cl_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
+        // Epilogue: TMEM -> registers (-> mask, add) -> bf16 -> 128B-swizzled staging
+        // block of 128 rows x 64 columns -> one TMA store per block (two staging
+        // buffers, so storing one block overlaps filling the next).
         const int quad = warp & 3;
+        const int er = quad * 32 + lane;   // row within this CTA's 128 rows (= TMEM lane)
+        const bool issuer = warp == 2 && lane == 0;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         uint32_t use = 0;
+        int sb = 0;
+        if (issuer) tma_prefetch_desc(&p.mapOut);
         for (int tile = pair; tile < total; tile += npairs) {
             const PairTile pt = pair_tile<BN>(tile, p);
             const Tail tl = tail_of(pt.mp, p);
@@ -257,13 +268,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint32_t b = C::kDouble ? (use & 1u) : 0u;
             const uint32_t full_parity = C::kDouble ? ((use >> 1) & 1u) : (use & 1u);
             const bool ok = mbar_wait_cl(&acc_full[b], full_parity, w, 4);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            // every epilogue thread has finished its (bounded) wait; all four warps
+            // leave together if any of them timed out or the CTA is aborting
+            if (named_barrier_or(1, 128, !ok || abort_flag != 0)) break;
             tc_fence_after();
-            const int64_t row = static_cast<int64_t>(m0) + quad * 32 + lane;
+            const int64_t row = static_cast<int64_t>(m0) + er;
             const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
             const uint32_t t1 = tmem + lane_off + b * C::kBufCols;
             const uint32_t t2 = t1 + BN;
-            uint16_t* out_row = p.out + row * p.N;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t v[32];
@@ -286,25 +298,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 } else {
                     tmem_ld_wait();
                 }
-                if (row < p.M) {
+                if (c == BN / 32 - 1) {
+                    // all of this tile's TMEM reads are done: hand the accumulator back
+                    tc_fence_before();
+                    mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+                }
+                const int half = c & 1;
+                uint8_t* buf = staging + sb * 16384;
+                if (half == 0) {
+                    // the store that last read this buffer (two blocks ago) must be done with it
+                    if (issuer) bulk_wait_read<1>();
+                    named_barrier(1, 128);
+                }
+                const uint32_t rowbase = smem_u32(buf) + er * 128;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int64_t col = static_cast<int64_t>(n0) + c * 32 + q * 8;
-                        if (col < p.N) {
-                            uint4 pk;
-                            pk.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
-                            pk.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
-                            pk.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
-                            pk.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
-                            stg128(out_row + col, pk);
-                        }
+                for (int q = 0; q < 4; ++q) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
+                    pk.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
+                    pk.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
+                    pk.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
+                    const int j = half * 4 + q;   // 16-byte chunk within the 128-byte row
+                    sts128(rowbase + ((j ^ (er & 7)) << 4), pk);
+                }
+                if (half == 1) {
+                    fence_proxy_async_smem();
+                    named_barrier(1, 128);
+                    if (issuer) {
+                        tma_store_2d(&p.mapOut, buf, n0 + (c - 1) * 32, m0);
+                        bulk_commit();
                     }
+                    sb ^= 1;
                 }
             }
-            tc_fence_before();
-            mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
             ++use;
         }
+        if (issuer) bulk_wait_all();
     }
 
     tc_fence_before();
@@ -319,7 +348,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 template <bool kBwd, int BN>
 size_t smem_bytes() {
     using C = Cfg<kBwd, BN>;
-    return 1024 + C::kStages * C::kStage + (2 * C::kStages + 5) * 8 + 16;
+    return 1024 + C::kStages * C::kStage + C::kStaging + (2 * C::kStages + 5) * 8 + 16;
 }
 
 }  // namespace

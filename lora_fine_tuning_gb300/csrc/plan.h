@@ -76,6 +76,7 @@ struct GemmParams {
     CUtensorMap mapB;                  // fwd: W {n, k} box {64, 64}; bwd: W {n, k} box {64, BN/2}
     CUtensorMap mapTA;                 // tail A: fwd S' / bwd dSq, {s_ld, m}, box {64, 128}
     CUtensorMap mapTB[kMaxAdapters];   // tail B: fwd B_i {n, r_i} box {64, 64}; bwd A_i {r_i, k} box {64, BN/2}
+    CUtensorMap mapOut;                // output Y / dX {N, M}, box {64, 128}, 128B swizzle (TMA store)
     Routing rt;
     DevCtl ctl;
     uint16_t* out;                     // Y (m x n) or dX (m x k), bf16
