@@ -4,9 +4,10 @@
 Default workload: the Llama-3.1-8B MLP up-projection shape, m=8192 tokens,
 k=4096, n=14336, rank 16, alpha 2, dropout 0.1, bf16 with fp32 accumulation,
 synthetic seeded inputs.  One step = lora_fwd + lora_bwd (every kernel of the
-hot path).  Prints one JSON line on rank 0.
+hot path); for the packed workload multi_4ad, multi_lora_fwd + multi_lora_bwd.
+Prints one JSON line on rank 0.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--m M] [--r R]
   python bench.py --impl reference     # the fp64 CPU oracle on the host cores
 
 N > 1 (torchrun): independent replicas, one per GPU, no collective on the data
@@ -49,21 +50,168 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_desc(name, cfg):
-    return (f"{name}: LoRA linear m={cfg['m']} tokens, k={cfg['k']}, n={cfg['n']}, r={cfg['r']}, "
-            f"alpha={cfg['alpha']}, p={cfg['p']}, seed={cfg['seed']}")
+MULTI = "multi_4ad"      # packed batch, four adapters with ranks 16/16/32/64 on one 8192x8192 weight
+LAYER = "llama8b_layer"  # the seven LoRA projections of one Llama-3.1-8B decoder layer
 
 
-def layer_flops(m, k, n, r):
-    """Algorithmic FLOPs of one fwd+bwd: 4mkn + 6mr(k+n) (no dW: W is frozen)."""
-    return 4 * m * k * n + 6 * m * r * (k + n)
+class Part:
+    """One LoRA linear of a workload: its shapes, weight, adapters, inputs and (packed) segments."""
+
+    def __init__(self, label, k, n, specs, seed, X, W, dY, adapters, segments=None, x_key="X"):
+        self.label, self.k, self.n, self.specs, self.seed = label, k, n, specs, seed
+        self.X, self.W, self.dY, self.adapters, self.segments, self.x_key = X, W, dY, adapters, segments, x_key
+
+    @property
+    def single(self) -> bool:
+        return self.segments is None
+
+    @property
+    def r_max(self) -> int:
+        return max(r for r, _, _ in self.specs)
 
 
-def layer_bytes(m, k, n, r):
-    """Compulsory HBM bytes of one fwd+bwd (bf16): fwd X, W, A, B, Y, S; bwd dY, W, X, S, A, B, dX, dA, dB."""
-    fwd = 2 * (m * k + k * n + k * r + r * n + m * n + m * r)
-    bwd = 2 * (m * n + k * n + m * k + m * r + k * r + r * n + m * k + k * r + r * n)
-    return fwd + bwd
+class Workload:
+    """One benchmark problem on the host: the token rows and one or more LoRA linears over them.
+
+    A single-adapter linear runs through lora_fwd / lora_bwd, the packed
+    multi-adapter one through multi_lora_fwd / multi_lora_bwd; the decoder
+    layer runs its seven linears forward in order, then backward in reverse.
+    """
+
+    def __init__(self, name: str, m=None, r=None):
+        self.name = name
+        if name == MULTI:
+            w = synth.MULTI_WORKLOAD
+            specs = [(s.rank, s.alpha, s.p) for s in w["specs"]]
+            batch = synth.packed_batch(w["seed"], m or w["total_rows"], len(specs))
+            self.m = batch.m
+            raw = synth.multi_inputs(w["seed"], w["k"], w["n"], w["specs"], batch)
+            self.owner = np.full(self.m, -1, dtype=np.int64)
+            valid = []
+            for (start, rows, a), v in zip(batch.segments, batch.valid):
+                self.owner[start:start + rows] = a
+                valid.append(np.arange(start, start + v))
+            self.valid_rows = np.concatenate(valid) if valid else np.zeros(0, dtype=np.int64)
+            self.parts = [Part("packed", w["k"], w["n"], specs, w["seed"], raw["X"], raw["W"], raw["dY"],
+                               raw["adapters"], list(batch.segments))]
+            self.n_samples = len(batch.segments)
+        elif name == LAYER:
+            cfg = dict(synth.LAYER_WORKLOAD)
+            self.m = m or cfg["m"]
+            r = r or cfg["r"]
+            raw = synth.decoder_layer_inputs(cfg["seed"], self.m, r)
+            self.parts = [Part(q["name"], q["k"], q["n"], [(r, cfg["alpha"], cfg["p"])], cfg["seed"] + i,
+                               raw["X"][q["input"]], q["W"], q["dY"], [(q["A"], q["B"])], x_key=q["input"])
+                          for i, q in enumerate(raw["parts"])]
+            self.owner = np.zeros(self.m, dtype=np.int64)
+            self.valid_rows = np.arange(self.m)
+        else:
+            cfg = dict(synth.WORKLOADS[name])
+            if m:
+                cfg["m"] = m
+            if r:
+                cfg["r"] = r
+            self.m = cfg["m"]
+            raw = synth.layer_inputs(cfg["seed"], self.m, cfg["k"], cfg["n"], cfg["r"])
+            self.parts = [Part(name, cfg["k"], cfg["n"], [(cfg["r"], cfg["alpha"], cfg["p"])], cfg["seed"],
+                               raw["X"], raw["W"], raw["dY"], [(raw["A"], raw["B"])])]
+            self.owner = np.zeros(self.m, dtype=np.int64)
+            self.valid_rows = np.arange(self.m)
+
+    @property
+    def tokens(self) -> int:
+        return int(self.valid_rows.size)
+
+    def tokens_of(self, i: int) -> int:
+        return int(np.count_nonzero(self.owner[self.valid_rows] == i))
+
+    def rows_of(self, i: int) -> int:
+        """Rows (padding included) the kernels run adapter i on."""
+        return int(np.count_nonzero(self.owner == i))
+
+    def describe(self) -> str:
+        if self.name == MULTI:
+            q = self.parts[0]
+            ads = ", ".join(f"(r={r}, alpha={a}, p={p})" for r, a, p in q.specs)
+            return (f"{self.name}: packed multi-adapter LoRA linear, {self.m} padded rows ({self.n_samples} samples, "
+                    f"lognormal lengths, {self.tokens} valid tokens), k={q.k}, n={q.n}, adapters {ads}, "
+                    f"seed={q.seed}")
+        if self.name == LAYER:
+            r, alpha, p = self.parts[0].specs[0]
+            shapes = ", ".join(f"{q.label} {q.k}x{q.n}" for q in self.parts)
+            return (f"{self.name}: the seven LoRA linears of a Llama-3.1-8B decoder layer ({shapes}), m={self.m} "
+                    f"tokens, r={r}, alpha={alpha}, p={p}; attention, norms and activations not included")
+        q = self.parts[0]
+        r, alpha, p = q.specs[0]
+        return f"{self.name}: LoRA linear m={self.m} tokens, k={q.k}, n={q.n}, r={r}, alpha={alpha}, p={p}, seed={q.seed}"
+
+    def layer_flops(self) -> int:
+        """Algorithmic FLOPs of one fwd+bwd over the valid tokens: per linear 4Tkn + sum_i 6 T_i r_i (k+n)
+        (W is frozen: no weight gradient)."""
+        F = 0
+        for q in self.parts:
+            F += 4 * self.tokens * q.k * q.n
+            F += sum(6 * self.tokens_of(i) * r * (q.k + q.n) for i, (r, _, _) in enumerate(q.specs))
+        return F
+
+    def layer_bytes(self) -> int:
+        """Compulsory bf16 HBM bytes of one fwd+bwd over the valid tokens.
+
+        Per linear, fwd: X, W, Y and per adapter A_i, B_i, S_i; bwd: dY, W, X,
+        dX and per adapter S_i, A_i, B_i, dA_i, dB_i.
+        """
+        T = self.tokens
+        total = 0
+        for q in self.parts:
+            k, n = q.k, q.n
+            fwd = T * k + k * n + T * n
+            bwd = T * n + k * n + 2 * T * k
+            for i, (r, _, _) in enumerate(q.specs):
+                Ti = self.tokens_of(i)
+                fwd += k * r + r * n + Ti * r
+                bwd += Ti * r + 2 * (k * r + r * n)
+            total += fwd + bwd
+        return 2 * total
+
+    def gemm_flops_per_step(self, kind: str):
+        """Algorithmic FLOPs of the frozen-weight GEMM launches of one kind (with their rank-r tails) in
+        one step, over the rows they run."""
+        if kind not in ("gemm_fwd", "gemm_bwd"):
+            return None
+        F = 0
+        for q in self.parts:
+            out = q.n if kind == "gemm_fwd" else q.k
+            F += 2 * self.m * q.k * q.n + sum(2 * self.rows_of(i) * r * out for i, (r, _, _) in enumerate(q.specs))
+        return F
+
+    def resident_bytes(self) -> int:
+        """Bytes of X, W, dY, Y and dX over all linears: what one step streams through L2."""
+        m = self.m
+        return sum(2 * (2 * m * q.k + q.k * q.n + 2 * m * q.n) for q in self.parts)
+
+
+def oracle_step(wl: Workload):
+    """fwd + bwd of the oracle on a sample of global rows of the workload (CPU legs only)."""
+    from oracle import lora_oracle as O
+    prepared = []
+    for q in wl.parts:
+        ads = [dict(A=O.bf16_to_f64(A), B=O.bf16_to_f64(B), alpha=a, p=p)
+               for (A, B), (_, a, p) in zip(q.adapters, q.specs)]
+        prepared.append((q, O.bf16_to_f64(q.W), ads))
+
+    def step(rows):
+        for q, W, ads in prepared:
+            X = O.bf16_to_f64(q.X[rows])
+            dY = O.bf16_to_f64(q.dY[rows])
+            if q.single:
+                ad = ads[0]
+                O.lora_forward(X, W, ad["A"], ad["B"], ad["alpha"], ad["p"], q.seed, rows=rows)
+                O.lora_backward(dY, X, W, ad["A"], ad["B"], ad["alpha"], ad["p"], q.seed, rows=rows)
+            else:
+                O.multi_lora_forward(X, W, ads, q.segments, q.seed, rows=rows)
+                O.multi_lora_backward(dY, X, W, ads, q.segments, q.seed, rows=rows)
+
+    return step
 
 
 def dist_env():
@@ -142,15 +290,15 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str):
-    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, or None if
+def profiled_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of `kernel` on `workload` from the committed ncu summary, or None if
     the kernel sources changed since the capture (or none exists)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         data = json.load(f)
-    entry = data.get(kernel)
+    entry = data.get(workload, {}).get(kernel)
     if not entry:
         return None
     if entry.get("source_digest") != source_digest(entry.get("sources", [])):
@@ -162,35 +310,27 @@ def profiled_traffic(kernel: str):
 # reference arm: the fp64 CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 
+def sample_rows(wl: Workload, rng, count: int):
+    count = int(np.clip(count, 1, wl.tokens))
+    return np.sort(rng.choice(wl.valid_rows, size=count, replace=False))
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    from oracle import lora_oracle as O
-    name = args.workload
-    cfg = synth.WORKLOADS[name]
-    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
-    raw = synth.layer_inputs(seed, m, k, n, r)
-    W = O.bf16_to_f64(raw["W"])
-    A = O.bf16_to_f64(raw["A"])
-    B = O.bf16_to_f64(raw["B"])
-
-    def step(rows):
-        X = O.bf16_to_f64(raw["X"][rows])
-        dY = O.bf16_to_f64(raw["dY"][rows])
-        O.lora_forward(X, W, A, B, alpha, p, seed, rows=rows)
-        O.lora_backward(dY, X, W, A, B, alpha, p, seed, rows=rows)
-
+    wl = Workload(args.workload, args.m, args.r)
+    step = oracle_step(wl)
     rng = np.random.default_rng(0)
-    probe = np.sort(rng.choice(m, size=32, replace=False))
+    probe = sample_rows(wl, rng, 32)
     t0 = time.perf_counter()
     step(probe)
     t_probe = time.perf_counter() - t0
     budget = min(args.ref_step_seconds, 150.0 / max(1, args.steps + args.warmup))
-    rows_per_step = int(np.clip(32 * budget / max(t_probe, 1e-3), 16, m))
+    rows_per_step = int(np.clip(probe.size * budget / max(t_probe, 1e-3), 16, wl.tokens))
     times = []
     for i in range(args.warmup + args.steps):
-        rows = np.sort(rng.choice(m, size=rows_per_step, replace=False))
+        rows = sample_rows(wl, rng, rows_per_step)
         t0 = time.perf_counter()
         step(rows)
         dt = time.perf_counter() - t0
@@ -199,81 +339,176 @@ def run_reference(args):
     total = sum(times)
     value = rows_per_step * len(times) / total
     cores = os.cpu_count()
-    sample = (f"{rows_per_step} random rows of the {m}-row batch per step (Y, S, dX rows and their dA/dB "
-              f"contributions; keep mask regenerated), fp64 numpy/BLAS")
+    sample = (f"{rows_per_step} random valid rows of the {wl.m}-row batch per step (Y, S, dX rows and their "
+              f"dA/dB contributions; keep mask regenerated), fp64 numpy/BLAS")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_desc(name, cfg), "parallelism": "host cores"},
+            "config": {"workload": wl.describe(), "parallelism": "host cores"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline_leg(name, cfg, seconds: float):
+def cpu_baseline_leg(wl: Workload, seconds: float):
     """The oracle as it stands on a bounded row sample of the same workload (rank 0, N=1)."""
-    from oracle import lora_oracle as O
-    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
-    raw = synth.layer_inputs(seed, m, k, n, r)
-    W, A, B = (O.bf16_to_f64(raw[x]) for x in ("W", "A", "B"))
+    step = oracle_step(wl)
     rng = np.random.default_rng(1)
-
-    def step(rows):
-        X = O.bf16_to_f64(raw["X"][rows])
-        dY = O.bf16_to_f64(raw["dY"][rows])
-        O.lora_forward(X, W, A, B, alpha, p, seed, rows=rows)
-        O.lora_backward(dY, X, W, A, B, alpha, p, seed, rows=rows)
-
-    probe = np.sort(rng.choice(m, size=32, replace=False))
+    probe = sample_rows(wl, rng, 32)
     t0 = time.perf_counter()
     step(probe)
     tp = time.perf_counter() - t0
-    rows_n = int(np.clip(32 * seconds / max(tp, 1e-3), 32, m))
-    rows = np.sort(rng.choice(m, size=rows_n, replace=False))
+    rows = sample_rows(wl, rng, int(probe.size * seconds / max(tp, 1e-3)))
     t0 = time.perf_counter()
     step(rows)
     dt = time.perf_counter() - t0
-    return {"value": rows_n / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{rows_n} of {m} rows, one fwd+bwd pass (fp64 numpy/BLAS), {dt:.1f} s"}
+    return {"value": rows.size / dt, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{rows.size} of {wl.tokens} valid rows, one fwd+bwd pass (fp64 numpy/BLAS), {dt:.1f} s"}
 
 
 # ---------------------------------------------------------------------------
 # native arm
 # ---------------------------------------------------------------------------
 
+class DeviceProblem:
+    """The workload's tensors on the GPU plus pinned host copies, and one step through the C ABI."""
+
+    def __init__(self, wl: Workload, dev, stream):
+        import torch
+
+        from lora_fine_tuning_gb300 import api
+        self.wl, self.dev, self.stream, self.api = wl, dev, stream, api
+        bf = torch.bfloat16
+
+        def pinned(a):
+            return torch.from_numpy(a.view(np.int16)).view(bf).pin_memory()
+
+        m = wl.m
+        self.inputs = {}   # name -> (pinned host, device); shared inputs appear once
+        self.parts = []
+        ws_need = (0, None)
+        for q in wl.parts:
+            if q.x_key not in self.inputs:
+                h = pinned(q.X)
+                self.inputs[q.x_key] = (h, h.to(dev))
+            dYh = pinned(q.dY)
+            self.inputs["dY:" + q.label] = (dYh, dYh.to(dev))
+            d = dict(part=q, X=self.inputs[q.x_key][1], dY=self.inputs["dY:" + q.label][1],
+                     W=pinned(q.W).to(dev), Y=torch.empty((m, q.n), dtype=bf, device=dev),
+                     dX=torch.empty((m, q.k), dtype=bf, device=dev),
+                     S=torch.empty((m, q.r_max), dtype=bf, device=dev),
+                     adapters=[api.Adapter(A=pinned(A).to(dev), B=pinned(B).to(dev), alpha=a, p=p,
+                                           dA=torch.empty((q.k, r), dtype=bf, device=dev),
+                                           dB=torch.empty((r, q.n), dtype=bf, device=dev))
+                               for (A, B), (r, a, p) in zip(q.adapters, q.specs)])
+            self.parts.append(d)
+            size = api.lora_workspace_size(m, q.k, q.n, max(8, q.r_max), len(q.adapters))
+            if size > ws_need[0]:
+                ws_need = (size, (m, q.k, q.n, max(8, q.r_max), len(q.adapters)))
+        self.ws = api.workspace(*ws_need[1], device=dev)
+
+    def _fwd(self, d):
+        api, q, s = self.api, d["part"], self.stream
+        if q.single:
+            a = d["adapters"][0]
+            api.lora_fwd(d["X"], d["W"], a.A, a.B, a.alpha, a.p, q.seed, Y=d["Y"], S_saved=d["S"], ws=self.ws,
+                         stream=s)
+        else:
+            api.multi_lora_fwd(d["X"], d["W"], d["adapters"], q.segments, q.seed, Y=d["Y"], S_saved=d["S"],
+                               ws=self.ws, stream=s)
+
+    def _bwd(self, d):
+        api, q, s = self.api, d["part"], self.stream
+        if q.single:
+            a = d["adapters"][0]
+            api.lora_bwd(d["dY"], d["X"], d["W"], a.A, a.B, d["S"], a.alpha, a.p, q.seed, dX=d["dX"], dA=a.dA,
+                         dB=a.dB, ws=self.ws, stream=s)
+        else:
+            api.multi_lora_bwd(d["dY"], d["X"], d["W"], d["adapters"], q.segments, q.seed, d["S"], dX=d["dX"],
+                               ws=self.ws, stream=s)
+
+    def step(self):
+        for d in self.parts:
+            self._fwd(d)
+        for d in reversed(self.parts):
+            self._bwd(d)
+
+    def frozen_step(self):
+        """The same linears with no adapter: Y = X W and dX = dY W^T through the same GEMM kernels."""
+        api, s = self.api, self.stream
+        for d in self.parts:
+            api.multi_lora_fwd(d["X"], d["W"], [], [], 0, Y=d["Y"], ws=self.ws, stream=s)
+        for d in reversed(self.parts):
+            api.multi_lora_bwd(d["dY"], d["X"], d["W"], [], [], 0, None, dX=d["dX"], ws=self.ws, stream=s)
+
+    def torch_frozen_step(self):
+        import torch
+        for d in self.parts:
+            torch.matmul(d["X"], d["W"], out=d["Y"])
+        for d in reversed(self.parts):
+            torch.matmul(d["dY"], d["W"].t(), out=d["dX"])
+
+    def outputs(self):
+        out = []
+        for d in self.parts:
+            out += [d["Y"], d["dX"]]
+            for a in d["adapters"]:
+                out += [a.dA, a.dB]
+        return out
+
+    def status(self) -> int:
+        return self.api.lora_device_status(self.ws, self.stream)
+
+
+def timed_loop(fn, steps, stream, flush=None):
+    """Device milliseconds of `steps` calls of fn, on `stream`.  With `flush`, L2 is overwritten
+    before every call and only the calls themselves are timed (per-call event pairs)."""
+    import torch
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    pairs = []
+    for _ in range(steps):
+        with torch.cuda.stream(stream):
+            flush.add_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        pairs.append((a, b))
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs)
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
 
-    from lora_fine_tuning_gb300 import api, native
+    from lora_fine_tuning_gb300 import native
 
     ws_n, rank, local = dist_env()
     if ws_n > 1 and not dist.is_initialized():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    name = args.workload
-    cfg = synth.WORKLOADS[name]
-    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
-
-    raw = synth.layer_inputs(seed, m, k, n, r)
-
-    def pinned(a):
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
-
-    Xh, Wh, Ah, Bh, dYh = (pinned(raw[x]) for x in ("X", "W", "A", "B", "dY"))
-    X, W, A, B, dY = (t.to(dev) for t in (Xh, Wh, Ah, Bh, dYh))
-    Y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
-    S = torch.empty((m, r), dtype=torch.bfloat16, device=dev)
-    dX = torch.empty((m, k), dtype=torch.bfloat16, device=dev)
-    dA = torch.empty((k, r), dtype=torch.bfloat16, device=dev)
-    dB = torch.empty((r, n), dtype=torch.bfloat16, device=dev)
-    wsb = api.workspace(m, k, n, r, device=dev)
+    wl = Workload(args.workload, args.m, args.r)
     stream = torch.cuda.current_stream(dev)
+    prob = DeviceProblem(wl, dev, stream)
 
-    def step():
-        api.lora_fwd(X, W, A, B, alpha, p, seed, Y=Y, S_saved=S, ws=wsb, stream=stream)
-        api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed, dX=dX, dA=dA, dB=dB, ws=wsb, stream=stream)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = None
+    if wl.resident_bytes() < 2 * l2_bytes:
+        flush = torch.empty(max(2 * l2_bytes, 256 << 20) // 4, dtype=torch.int32, device=dev)
+        l2_note = (f"L2 flushed before every step (write of a {flush.numel() * 4 >> 20} MiB buffer, outside the "
+                   f"timed events): X/W/dY/Y/dX total {wl.resident_bytes() / 1e6:.0f} MB")
+    else:
+        l2_note = (f"no flush: X/W/dY/Y/dX total {wl.resident_bytes() / 1e6:.0f} MB, larger than twice L2 "
+                   f"({l2_bytes >> 20} MiB)")
 
     def barrier():
         if ws_n > 1:
@@ -287,95 +522,65 @@ def run_native(args):
         return float(t.item())
 
     for _ in range(args.warmup):
-        step()
+        prob.step()
     torch.cuda.synchronize(dev)
-    if api.lora_device_status(wsb, stream) != 0:
+    if prob.status() != 0:
         raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
 
     # --- timed region (device, inputs resident in HBM; per-kernel events on the launch stream) ---
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize(dev)
         native.timing_begin()
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        elapsed_ms = timed_loop(prob.step, args.steps, stream, flush)
         kernel_times = native.timing_end()
         barrier()
-    elapsed_ms = max_over_ranks(e0.elapsed_time(e1))
+    elapsed_ms = max_over_ranks(elapsed_ms)
     clk = clocks.summary()
-    if api.lora_device_status(wsb, stream) != 0:
+    if prob.status() != 0:
         raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
 
     ms_per_step = elapsed_ms / args.steps
-    tokens = m * args.steps * ws_n
-    value = tokens / (elapsed_ms / 1e3)
+    value = wl.tokens * args.steps * ws_n / (elapsed_ms / 1e3)
 
     # --- end to end through the public API with host buffers ---
     e2e = None
     if not args.no_e2e:
-        Yh = torch.empty((m, n), dtype=torch.bfloat16).pin_memory()
-        dXh = torch.empty((m, k), dtype=torch.bfloat16).pin_memory()
-        dAh = torch.empty((k, r), dtype=torch.bfloat16).pin_memory()
-        dBh = torch.empty((r, n), dtype=torch.bfloat16).pin_memory()
+        outs = prob.outputs()
+        hosts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
         e2e_steps = max(3, min(args.steps, 20))
 
         def e2e_step():
-            X.copy_(Xh, non_blocking=True)
-            dY.copy_(dYh, non_blocking=True)
-            step()
-            Yh.copy_(Y, non_blocking=True)
-            dXh.copy_(dX, non_blocking=True)
-            dAh.copy_(dA, non_blocking=True)
-            dBh.copy_(dB, non_blocking=True)
+            for h, t in prob.inputs.values():
+                t.copy_(h, non_blocking=True)
+            prob.step()
+            for h, t in zip(hosts, outs):
+                h.copy_(t, non_blocking=True)
 
         e2e_step()
         torch.cuda.synchronize(dev)
         barrier()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        f1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(f0.elapsed_time(f1))
-        h2d = (Xh.numel() + dYh.numel()) * 2
-        d2h = (Yh.numel() + dXh.numel() + dAh.numel() + dBh.numel()) * 2
-        e2e = {"value": m * e2e_steps * ws_n / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks(timed_loop(e2e_step, e2e_steps, stream))
+        h2d = sum(h.numel() * h.element_size() for h, _ in prob.inputs.values())
+        d2h = sum(h.numel() * h.element_size() for h in hosts)
+        e2e = {"value": wl.tokens * e2e_steps * ws_n / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps}
 
     # --- frozen-layer reference points (overhead of the LoRA branch) ---
     frozen = None
     if not args.no_frozen:
         reps = args.steps   # same length as the timed LoRA loop, so both see the same clock behaviour
-
-        def frozen_ours():
-            api.multi_lora_fwd(X, W, [], [], seed, Y=Y, ws=wsb, stream=stream)
-            api.multi_lora_bwd(dY, X, W, [], [], seed, None, dX=dX, ws=wsb, stream=stream)
-
-        def frozen_torch():
-            torch.matmul(X, W, out=Y)
-            torch.matmul(dY, W.t(), out=dX)
-
         res = {}
         frozen_kernels = {}
-        for label, fn in (("ours", frozen_ours), ("torch_matmul", frozen_torch)):
+        for label, fn in (("ours", prob.frozen_step), ("torch_matmul", prob.torch_frozen_step)):
             fn()
             torch.cuda.synchronize(dev)
             if label == "ours":
                 native.timing_begin()
-            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            g0.record(stream)
-            for _ in range(reps):
-                fn()
-            g1.record(stream)
-            torch.cuda.synchronize(dev)
+            ms = timed_loop(fn, reps, stream, flush)
             if label == "ours":
-                frozen_kernels = {kname: ms / max(1, cnt) for kname, (ms, cnt) in native.timing_end().items()}
-            res[label] = max_over_ranks(g0.elapsed_time(g1)) / reps
+                frozen_kernels = {kname: t / max(1, cnt) for kname, (t, cnt) in native.timing_end().items()}
+            res[label] = max_over_ranks(ms) / reps
         frozen = {"frozen_ms_per_step_ours": res["ours"], "frozen_ms_per_step_torch": res["torch_matmul"],
                   "frozen_ms_per_launch_ours": frozen_kernels,
                   "lora_overhead_vs_ours": ms_per_step / res["ours"],
@@ -386,47 +591,40 @@ def run_native(args):
 
     peaks, peak_kind = load_peaks()
     # dominant kernel: the largest summed device time
-    dom = max(kernel_times.items(), key=lambda kv: kv[1][0])
-    dom_name, (dom_ms, dom_launches) = dom
-    avg_ms = dom_ms / max(1, dom_launches)
-    if dom_name == "gemm_bwd":
-        dom_flops = 2 * m * n * k + 2 * m * r * k
-    elif dom_name == "gemm_fwd":
-        dom_flops = 2 * m * k * n + 2 * m * r * n
-    else:
-        dom_flops = None
+    dom_name, (dom_ms, dom_launches) = max(kernel_times.items(), key=lambda kv: kv[1][0])
+    dom_flops = wl.gemm_flops_per_step(dom_name)
     if dom_flops is not None:
-        achieved = dom_flops / (avg_ms / 1e3) / 1e12
+        # FLOPs of all its launches over their summed device time (one launch per step for one linear)
+        achieved = dom_flops * args.steps / (dom_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
         roofline = {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                    "frac": achieved / peak, "traffic": profiled_traffic(dom_name),
+                    "frac": achieved / peak, "traffic": profiled_traffic(dom_name, wl.name),
                     "peak_source": f"{peak_kind} (burst bf16)",
                     "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak)}
     else:
         roofline = {"bound": "hbm", "kernel": dom_name, "achieved": None, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": None, "traffic": None}
 
-    F = layer_flops(m, k, n, r)
-    Bc = layer_bytes(m, k, n, r)
+    F, Bc = wl.layer_flops(), wl.layer_bytes()
     t_roof = max(F / (peaks["bf16_tflops"] * 1e12), Bc / (peaks["hbm_gbs"] * 1e9))
     layer_roof = {"flops": F, "compulsory_bytes": Bc, "roofline_ms": t_roof * 1e3,
                   "frac": t_roof * 1e3 / ms_per_step, "peak_source": peak_kind,
                   "achieved_tflops": F / (ms_per_step / 1e3) / 1e12}
 
-    kernels = {kname: {"ms_per_launch": ms / max(1, cnt), "launches": cnt, "share": ms / max(1e-9, elapsed_ms)}
-               for kname, (ms, cnt) in sorted(kernel_times.items(), key=lambda kv: -kv[1][0])}
-    gpu_launches = sum(cnt for kname, (ms, cnt) in kernel_times.items() if kname != "memset")
+    kernels = {kname: {"ms_per_launch": t / max(1, cnt), "launches": cnt, "share": t / max(1e-9, elapsed_ms)}
+               for kname, (t, cnt) in sorted(kernel_times.items(), key=lambda kv: -kv[1][0])}
+    gpu_launches = sum(cnt for kname, (t, cnt) in kernel_times.items() if kname != "memset")
 
     cpu = None
     if ws_n == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_leg(name, cfg, args.cpu_seconds)
+        cpu = cpu_baseline_leg(wl, args.cpu_seconds)
 
+    config = {"workload": wl.describe(), "m": wl.m, "k": [q.k for q in wl.parts], "n": [q.n for q in wl.parts],
+              "r": [[r for r, _, _ in q.specs] for q in wl.parts], "tokens_per_step": wl.tokens,
+              "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU", "l2": l2_note}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, Llama-shaped)",
-            "config": {"workload": workload_desc(name, cfg), "m": m, "k": k, "n": n, "r": r,
-                       "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU",
-                       "l2": "no flush: inputs larger than L2 (X 67 MB, W 117 MB, dY 235 MB, Y/dX written)"},
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, Llama-shaped)", "config": config,
             "roofline": roofline, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": gpu_launches, "kernels": kernels, "clocks": clk}
     if frozen:
@@ -440,8 +638,10 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--m", type=int, default=None, help="override the workload's token count (profiling runs)")
+    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, LAYER])
+    ap.add_argument("--m", type=int, default=None,
+                    help="override the workload's token count (padded rows for the packed workload)")
+    ap.add_argument("--r", type=int, default=None, help="override the rank of a single-adapter workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline leg")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -450,8 +650,6 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.m is not None:
-        synth.WORKLOADS[args.workload] = dict(synth.WORKLOADS[args.workload], m=args.m)
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -147,7 +147,41 @@ WORKLOADS = {
     "llama70b_o_r64": dict(m=16384, k=8192, n=8192, r=64, alpha=2.0, p=0.1, seed=2),
     "llama70b_up_r16": dict(m=16384, k=8192, n=28672, r=16, alpha=2.0, p=0.1, seed=2),
     "llama70b_up_r64": dict(m=16384, k=8192, n=28672, r=64, alpha=2.0, p=0.1, seed=2),
+    # square 4096 layer for sweeps over the token count and the rank
+    "square4096": dict(m=4096, k=4096, n=4096, r=16, alpha=2.0, p=0.1, seed=4),
 }
+
+# all seven projections of a Llama-3.1-8B decoder layer, one adapter each
+LAYER_WORKLOAD = dict(m=8192, r=16, alpha=2.0, p=0.1, seed=5)
+
+# The seven projections of one Llama-3.1-8B decoder layer (hidden 4096, MLP 14336,
+# 32 query heads and 8 key/value heads of width 128): (name, k, n, input).  The
+# projections that read the same activation share it: q/k/v the attention input,
+# gate/up the MLP input.
+LLAMA8B_LAYER = [("q_proj", 4096, 4096, "attn_in"), ("k_proj", 4096, 1024, "attn_in"),
+                 ("v_proj", 4096, 1024, "attn_in"), ("o_proj", 4096, 4096, "attn_out"),
+                 ("gate_proj", 4096, 14336, "mlp_in"), ("up_proj", 4096, 14336, "mlp_in"),
+                 ("down_proj", 14336, 4096, "mlp_act")]
+
+
+def decoder_layer_inputs(seed: int, m: int, r: int):
+    """Inputs of the seven LoRA linears of one decoder layer for m tokens.
+
+    Returns {"X": {input name: m x k}, "parts": [dict(name, k, n, input, W, A, B, dY)]},
+    every tensor seeded from `seed` and the projection's position.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    xs = {}
+    for _name, k, _n, src in LLAMA8B_LAYER:
+        if src not in xs:
+            xs[src] = _normal(rng, (m, k), 1.0)
+    parts = []
+    for name, k, n, src in LLAMA8B_LAYER:
+        W = _normal(rng, (k, n), 1.0 / math.sqrt(k))
+        A, B = adapter_weights(rng, k, n, r)
+        parts.append(dict(name=name, k=k, n=n, input=src, W=W, A=A, B=B, dY=_normal(rng, (m, n), 1.0)))
+    return {"X": xs, "parts": parts}
+
 
 MULTI_WORKLOAD = dict(k=8192, n=8192, total_rows=16384, seed=3,
                       specs=[AdapterSpec(16, 1.0, 0.0), AdapterSpec(16, 2.0, 0.1),

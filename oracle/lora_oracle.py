@@ -284,16 +284,24 @@ def multi_lora_forward(X, W, adapters, segments, seed: int, rows=None):
     return Y, S_list, owner
 
 
-def multi_lora_backward(dY, X, W, adapters, segments, seed: int):
+def multi_lora_backward(dY, X, W, adapters, segments, seed: int, rows=None):
     """Packed multi-adapter backward.  Returns (dX, dA_list, dB_list, dS_list, owner).
 
     dA_i and dB_i sum over the rows of adapter i only; an adapter with no rows
-    gets zero gradients.
+    gets zero gradients.  `rows` restricts the computation to those global rows
+    (dX for them, and their share of each dA_i / dB_i), as in the forward.
     """
     X = np.asarray(X, dtype=np.float64)
     dY = np.asarray(dY, dtype=np.float64)
-    m = X.shape[0]
-    owner = row_adapters(segments, m, len(adapters))
+    m_total = None
+    if rows is None:
+        rows = np.arange(X.shape[0])
+        m_total = X.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    if m_total is None:
+        m_total = int(rows.max()) + 1 if rows.size else 0
+        m_total = max(m_total, max((s + r for s, r, _ in segments), default=0))
+    owner = row_adapters(segments, m_total, len(adapters))[rows]
     dX = dY @ W.T
     dA_list, dB_list, dS_list = [], [], []
     for i, ad in enumerate(adapters):
@@ -304,7 +312,7 @@ def multi_lora_backward(dY, X, W, adapters, segments, seed: int):
             dB_list.append(np.zeros_like(B, dtype=np.float64))
             dS_list.append(np.zeros((0, A.shape[1])))
             continue
-        dXi, dAi, dBi, dSi = lora_branch_backward(dY[sel], X[sel], A, B, ad["alpha"], ad["p"], seed, sel)
+        dXi, dAi, dBi, dSi = lora_branch_backward(dY[sel], X[sel], A, B, ad["alpha"], ad["p"], seed, rows[sel])
         dX[sel] += dXi
         dA_list.append(dAi)
         dB_list.append(dBi)

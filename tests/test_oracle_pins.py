@@ -318,6 +318,29 @@ def test_multi_matches_per_row_brute_force():
     assert not dA[2].any() and not dB[2].any()
 
 
+def test_multi_backward_on_row_subsets_adds_up():
+    """Restricting the packed backward to rows: dX rows agree with the full pass and each dA_i / dB_i
+    is the sum of its parts over a partition of the rows (sums over rows, by the definition)."""
+    X, W, dY, adapters, segments = multi_problem(3)
+    m = X.shape[0]
+    seed = 99
+    dX, dA, dB, _, _ = O.multi_lora_backward(dY, X, W, adapters, segments, seed)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(m)
+    parts = [np.sort(perm[: m // 3]), np.sort(perm[m // 3:])]
+    dA_sum = [np.zeros_like(a["A"]) for a in adapters]
+    dB_sum = [np.zeros_like(a["B"]) for a in adapters]
+    for rows in parts:
+        dXp, dAp, dBp, _, owner = O.multi_lora_backward(dY[rows], X[rows], W, adapters, segments, seed, rows=rows)
+        np.testing.assert_allclose(dXp, dX[rows], rtol=1e-12, atol=1e-12)
+        for i in range(len(adapters)):
+            dA_sum[i] += dAp[i]
+            dB_sum[i] += dBp[i]
+    for i in range(len(adapters)):
+        np.testing.assert_allclose(dA_sum[i], dA[i], rtol=1e-10, atol=1e-10)
+        np.testing.assert_allclose(dB_sum[i], dB[i], rtol=1e-10, atol=1e-10)
+
+
 def test_tile_table_brute_force():
     segments = [(0, 128, 1), (256, 256, 0), (512, 128, 3)]
     tiles = O.tile_adapters(segments, 700, 4)
