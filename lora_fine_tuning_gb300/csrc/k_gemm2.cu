@@ -196,6 +196,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             uint32_t use = 0;
             const uint32_t idesc = make_idesc_bf16(256, BN, false, !kBwd);
+            // operand descriptors of stage 0 at K step 0; stage s and K step ks (16 deep) only move the
+            // start-address field (bytes / 16): by s * stage bytes, and by 32 B (K-major) or 2048 B
+            // (MN-major B: 16 rows of 128 B) per step; shared-memory addresses stay below 256 KB,
+            // so the 14-bit field never carries
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t a_desc0 = make_smem_desc(sbase, 16, 1024, kSw128);
+            const uint64_t b_desc0 = kBwd ? make_smem_desc(sbase + C::kA, 16, 1024, kSw128)
+                                          : make_smem_desc(sbase + C::kA, 8192, 1024, kSw128);
+            constexpr uint64_t kBStep = kBwd ? 2u : 128u;
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const PairTile pt = pair_tile<BN>(tile, p);
@@ -206,35 +215,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t acc1 = tmem + b * C::kBufCols;
                 const uint32_t acc2 = acc1 + BN;
-                for (int kb = 0; kb < p.nkb + tl.total; ++kb) {
+                for (int kb = 0; kb < p.nkb; ++kb) {
                     if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t as = smem_u32(smem + s * C::kStage);
-                    const uint32_t bs = as + C::kA;
-                    if (kb < p.nkb) {
+                    const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
+                    umma_bf16_pair(acc1, a_desc0 + so, b_desc0 + so, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            const uint64_t ad = make_smem_desc(as + ks * 32, 16, 1024, kSw128);
-                            const uint64_t bd = kBwd ? make_smem_desc(bs + ks * 32, 16, 1024, kSw128)
-                                                     : make_smem_desc(bs + ks * 2048, 8192, 1024, kSw128);
-                            umma_bf16_pair(acc1, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
-                        }
-                    } else {
-                        const int t = kb - p.nkb;
-                        const int pass = t < tl.nb[0] ? 0 : 1;
-                        const int tb = pass == 0 ? t : t - tl.nb[0];
-                        const int left = p.rt.ad[tl.a[pass]].rank - tb * 64;
-                        const int nks = left >= 64 ? 4 : (left + 15) / 16;
-                        for (int ks = 0; ks < nks; ++ks) {
-                            const uint64_t ad = make_smem_desc(as + ks * 32, 16, 1024, kSw128);
-                            if (kBwd) {
-                                const uint64_t bd = make_smem_desc(bs + ks * 32, 16, 1024, kSw128);
-                                umma_bf16_pair(acc2, ad, bd, idesc, (t | ks) != 0 ? 1u : 0u);
-                            } else {
-                                const uint64_t bd = make_smem_desc(bs + ks * 2048, 8192, 1024, kSw128);
-                                umma_bf16_pair(acc1, ad, bd, idesc, 1u);
-                            }
-                        }
+                    for (int ks = 1; ks < 4; ++ks)
+                        umma_bf16_pair(acc1, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc, 1u);
+                    umma_commit_pair(&empty[s], 3);
+                    if (++s == S) { s = 0; ph ^= 1u; }
+                }
+                for (int t = 0; t < tl.total && ok; ++t) {
+                    if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
+                    const int pass = t < tl.nb[0] ? 0 : 1;
+                    const int tb = pass == 0 ? t : t - tl.nb[0];
+                    const int left = p.rt.ad[tl.a[pass]].rank - tb * 64;
+                    const int nks = left >= 64 ? 4 : (left + 15) / 16;
+                    for (int ks = 0; ks < nks; ++ks) {
+                        if (kBwd)
+                            umma_bf16_pair(acc2, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc,
+                                           (t | ks) != 0 ? 1u : 0u);
+                        else
+                            umma_bf16_pair(acc1, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc, 1u);
                     }
                     umma_commit_pair(&empty[s], 3);
                     if (++s == S) { s = 0; ph ^= 1u; }
@@ -247,9 +252,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mbar_wait_cl_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // Epilogue: TMEM -> registers (-> mask, add) -> bf16 -> 128B-swizzled staging
-        // block of 128 rows x 64 columns -> one TMA store per block (two staging
-        // buffers, so storing one block overlaps filling the next).
+        // Epilogue.  While the tile's MMAs run: the keep bits of this thread's row
+        // (backward).  Then TMEM -> registers (-> mask, add) -> packed bf16 for the
+        // whole 128 x BN tile, and the accumulator goes back to the MMA warp before
+        // anything is stored.  Then 128B-swizzled staging blocks of 128 rows x 64
+        // columns, one TMA store each (two staging buffers, so storing one block
+        // overlaps filling the next).
         const int quad = warp & 3;
         const int er = quad * 32 + lane;   // row within this CTA's 128 rows (= TMEM lane)
         const bool issuer = warp == 2 && lane == 0;
@@ -264,7 +272,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int n0 = pt.np * BN;
             const int a = tl.half_adapter[rank];
             const bool branch = kBwd && a >= 0;
-            const uint32_t T = a >= 0 ? p.rt.ad[a].T : 0u;
+            const int64_t row = static_cast<int64_t>(m0) + er;
+            uint32_t keep[BN / 32];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) keep[c] = 0u;
+            if (branch) {
+                const uint32_t T = p.rt.ad[a].T;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        const uint32_t grp = static_cast<uint32_t>((n0 + c * 32 + g * 8) >> 3);
+                        keep[c] |= keep_byte(philox_10(static_cast<uint32_t>(row), grp, keys), T) << (8 * g);
+                    }
+                }
+            }
             const uint32_t b = C::kDouble ? (use & 1u) : 0u;
             const uint32_t full_parity = C::kDouble ? ((use >> 1) & 1u) : (use & 1u);
             const bool ok = mbar_wait_cl(&acc_full[b], full_parity, w, 4);
@@ -272,64 +294,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // leave together if any of them timed out or the CTA is aborting
             if (named_barrier_or(1, 128, !ok || abort_flag != 0)) break;
             tc_fence_after();
-            const int64_t row = static_cast<int64_t>(m0) + er;
             const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
             const uint32_t t1 = tmem + lane_off + b * C::kBufCols;
             const uint32_t t2 = t1 + BN;
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t1 + c * 32, v);
+            uint32_t packed[BN / 2];
+#pragma unroll
+            for (int c = 0; c < BN / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(t1 + c * 16, v);
                 if (branch) {
-                    uint32_t u[32];
-                    tmem_ld32(t2 + c * 32, u);
+                    uint32_t u[16];
+                    tmem_ld16(t2 + c * 16, u);
                     tmem_ld_wait();
+                    const uint32_t kb = keep[c >> 1] >> ((c & 1) * 16);
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int64_t col0 = static_cast<int64_t>(n0) + c * 32 + g * 8;
-                        const uint4 wv = philox_10(static_cast<uint32_t>(row), static_cast<uint32_t>(col0 >> 3), keys);
-                        const uint32_t keep = keep_byte(wv, T);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            if ((keep >> e) & 1u)
-                                v[g * 8 + e] =
-                                    __float_as_uint(__uint_as_float(v[g * 8 + e]) + __uint_as_float(u[g * 8 + e]));
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        if ((kb >> e) & 1u)
+                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
                 } else {
                     tmem_ld_wait();
                 }
-                if (c == BN / 32 - 1) {
-                    // all of this tile's TMEM reads are done: hand the accumulator back
-                    tc_fence_before();
-                    mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
-                }
-                const int half = c & 1;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    packed[c * 8 + e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+            }
+            // all of this tile's TMEM reads are done: hand the accumulator back
+            tc_fence_before();
+            mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+#pragma unroll
+            for (int blk = 0; blk < BN / 64; ++blk) {
                 uint8_t* buf = staging + sb * 16384;
-                if (half == 0) {
-                    // the store that last read this buffer (two blocks ago) must be done with it
-                    if (issuer) bulk_wait_read<1>();
-                    named_barrier(1, 128);
-                }
+                // the store that last read this buffer (two blocks ago) must be done with it
+                if (issuer) bulk_wait_read<1>();
+                named_barrier(1, 128);
                 const uint32_t rowbase = smem_u32(buf) + er * 128;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 pk;
-                    pk.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]), __uint_as_float(v[q * 8 + 1]));
-                    pk.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]), __uint_as_float(v[q * 8 + 3]));
-                    pk.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]), __uint_as_float(v[q * 8 + 5]));
-                    pk.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]), __uint_as_float(v[q * 8 + 7]));
-                    const int j = half * 4 + q;   // 16-byte chunk within the 128-byte row
+                for (int j = 0; j < 8; ++j) {   // 16-byte chunk j of the row's 128 bytes
+                    const uint4 pk = make_uint4(packed[blk * 32 + j * 4 + 0], packed[blk * 32 + j * 4 + 1],
+                                                packed[blk * 32 + j * 4 + 2], packed[blk * 32 + j * 4 + 3]);
                     sts128(rowbase + ((j ^ (er & 7)) << 4), pk);
                 }
-                if (half == 1) {
-                    fence_proxy_async_smem();
-                    named_barrier(1, 128);
-                    if (issuer) {
-                        tma_store_2d(&p.mapOut, buf, n0 + (c - 1) * 32, m0);
-                        bulk_commit();
-                    }
-                    sb ^= 1;
+                fence_proxy_async_smem();
+                named_barrier(1, 128);
+                if (issuer) {
+                    tma_store_2d(&p.mapOut, buf, n0 + blk * 64, m0);
+                    bulk_commit();
                 }
+                sb ^= 1;
             }
             ++use;
         }

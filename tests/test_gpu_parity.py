@@ -194,10 +194,11 @@ def test_multi_with_one_adapter_equals_single():
     dX2 = api.multi_lora_bwd(dY, X, W, ad, [(0, m, 0)], seed, S2)
     torch.cuda.synchronize()
     assert torch.equal(M1, M2)
-    # same kernels and routing; values agree up to the order of the fp32 split-K reductions
-    assert_close("Y", host_f64(Y2), host_f64(Y1), 1e-3)
-    assert_close("S", host_f64(S2), host_f64(S1), 1e-3)
-    assert_close("dX", host_f64(dX2), host_f64(dX1), 1e-3)
+    # same kernels and routing; values agree up to the order of the fp32 split-K reductions, which
+    # can move a bf16 rounding of S (and through it of Y, dX) by one unit: 2^-8 of the value
+    assert_close("Y", host_f64(Y2), host_f64(Y1), 4e-3)
+    assert_close("S", host_f64(S2), host_f64(S1), 4e-3)
+    assert_close("dX", host_f64(dX2), host_f64(dX1), 4e-3)
     # dA, dB pass through dSq (bf16, reduced with atomics): agreement within the parity tolerance
     assert_close("dA", host_f64(ad[0].dA), host_f64(dA1), TOL)
     assert_close("dB", host_f64(ad[0].dB), host_f64(dB1), TOL)
