@@ -33,12 +33,15 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kGroupPairs = 8;   // rasterisation: pair-rows per group
+constexpr int kBK = 64;          // K depth of one pipeline stage (a multiple of 64: one 128-byte swizzle row)
+constexpr int kKB = kBK / 64;    // 64-deep TMA boxes per operand and stage
 
 template <bool kBwd, int BN>
 struct Cfg {
     static constexpr int BNH = BN / 2;                        // B columns (fwd) / rows (bwd) per CTA
-    static constexpr uint32_t kA = 128u * 128u;                // 128 rows x 64 bf16
-    static constexpr uint32_t kB = static_cast<uint32_t>(BNH) * 128u;
+    static constexpr uint32_t kA = 128u * 128u * kKB;          // 128 rows x kBK bf16 (kKB boxes of 16 KB)
+    static constexpr uint32_t kBox = static_cast<uint32_t>(BNH) * 128u;   // B: BNH x 64 bf16
+    static constexpr uint32_t kB = kBox * kKB;
     static constexpr uint32_t kStage = kA + kB;
     static constexpr int kStages = (192 * 1024) / kStage > 8 ? 8 : (192 * 1024) / kStage;
     static constexpr uint32_t kStaging = 2u * 16384u;           // two 128 x 64 bf16 output buffers
@@ -52,7 +55,7 @@ struct PairTile {
 
 struct Tail {
     int a[2];    // adapter of each pass (-1: none)
-    int nb[2];   // 64-deep blocks of each pass
+    int nb[2];   // kBK-deep blocks of each pass
     int total;
     int half_adapter[2];   // adapter of each 128-row half
 };
@@ -66,7 +69,7 @@ __device__ __forceinline__ Tail tail_of(int mp, const GemmParams& p) {
     t.half_adapter[1] = a1;
     t.a[0] = a0 >= 0 ? a0 : a1;
     t.a[1] = (a0 >= 0 && a1 >= 0 && a1 != a0) ? a1 : -1;
-    for (int i = 0; i < 2; ++i) t.nb[i] = t.a[i] >= 0 ? (p.rt.ad[t.a[i]].rank + 63) / 64 : 0;
+    for (int i = 0; i < 2; ++i) t.nb[i] = t.a[i] >= 0 ? (p.rt.ad[t.a[i]].rank + kBK - 1) / kBK : 0;
     t.total = t.nb[0] + t.nb[1];
     return t;
 }
@@ -137,6 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int total = n_mp * n_np;
     const int pair = blockIdx.x >> 1;
     const int npairs = gridDim.x >> 1;
+    const int nkb = (p.nkb + kKB - 1) / kKB;   // kBK-deep stages of the main loop (p.nkb counts 64-deep blocks)
 
     if (warp == 0) {
         if (lane == 0) {
@@ -150,34 +154,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int n0 = pt.np * BN + static_cast<int>(rank) * C::BNH;
                 const Tail tl = tail_of(pt.mp, p);
                 const int my_adapter = tl.half_adapter[rank];
-                for (int kb = 0; kb < p.nkb + tl.total; ++kb) {
+                for (int kb = 0; kb < nkb + tl.total; ++kb) {
                     if (!mbar_wait_cl(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                     uint8_t* as = smem + s * C::kStage;
                     uint8_t* bs = as + C::kA;
                     if (leader) mbar_arrive_expect_tx(&full[s], 2u * C::kStage);
                     const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
-                    if (kb < p.nkb) {
-                        tma_load_2d_pair(as, &p.mapA, fb, kb * 64, m0);
-                        if (kBwd) {
-                            tma_load_2d_pair(bs, &p.mapB, fb, kb * 64, n0);
-                        } else {
+                    // kKB boxes of 64 K per operand; a box past the end of K reads zeros
+                    if (kb < nkb) {
 #pragma unroll
-                            for (int j = 0; j < C::BNH / 64; ++j)
-                                tma_load_2d_pair(bs + j * 8192, &p.mapB, fb, n0 + 64 * j, kb * 64);
+                        for (int q = 0; q < kKB; ++q) {
+                            const int x = kb * kBK + 64 * q;
+                            tma_load_2d_pair(as + q * 16384, &p.mapA, fb, x, m0);
+                            if (kBwd) {
+                                tma_load_2d_pair(bs + q * C::kBox, &p.mapB, fb, x, n0);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < C::BNH / 64; ++j)
+                                    tma_load_2d_pair(bs + q * C::kBox + j * 8192, &p.mapB, fb, n0 + 64 * j, x);
+                            }
                         }
                     } else {
-                        const int t = kb - p.nkb;
+                        const int t = kb - nkb;
                         const int pass = t < tl.nb[0] ? 0 : 1;
                         const int tb = pass == 0 ? t : t - tl.nb[0];
                         const int a = tl.a[pass];
-                        // rows of the other adapter's half read zeros (box wholly outside the tensor)
-                        tma_load_2d_pair(as, &p.mapTA, fb, tb * 64, my_adapter == a ? m0 : -256);
-                        if (kBwd) {
-                            tma_load_2d_pair(bs, &p.mapTB[a], fb, tb * 64, n0);
-                        } else {
 #pragma unroll
-                            for (int j = 0; j < C::BNH / 64; ++j)
-                                tma_load_2d_pair(bs + j * 8192, &p.mapTB[a], fb, n0 + 64 * j, tb * 64);
+                        for (int q = 0; q < kKB; ++q) {
+                            const int x = tb * kBK + 64 * q;
+                            // rows of the other adapter's half read zeros (box wholly outside the tensor)
+                            tma_load_2d_pair(as + q * 16384, &p.mapTA, fb, x, my_adapter == a ? m0 : -256);
+                            if (kBwd) {
+                                tma_load_2d_pair(bs + q * C::kBox, &p.mapTB[a], fb, x, n0);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < C::BNH / 64; ++j)
+                                    tma_load_2d_pair(bs + q * C::kBox + j * 8192, &p.mapTB[a], fb, n0 + 64 * j, x);
+                            }
                         }
                     }
                     ++issued;
@@ -197,14 +210,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t use = 0;
             const uint32_t idesc = make_idesc_bf16(256, BN, false, !kBwd);
             // operand descriptors of stage 0 at K step 0; stage s and K step ks (16 deep) only move the
-            // start-address field (bytes / 16): by s * stage bytes, and by 32 B (K-major) or 2048 B
-            // (MN-major B: 16 rows of 128 B) per step; shared-memory addresses stay below 256 KB,
-            // so the 14-bit field never carries
+            // start-address field (bytes / 16): by s * stage bytes, by the 64-deep box ks / 4, and
+            // within it by 32 B (K-major) or 2048 B (MN-major B: 16 rows of 128 B) per step;
+            // shared-memory addresses stay below 256 KB, so the 14-bit field never carries
             const uint32_t sbase = smem_u32(smem);
             const uint64_t a_desc0 = make_smem_desc(sbase, 16, 1024, kSw128);
             const uint64_t b_desc0 = kBwd ? make_smem_desc(sbase + C::kA, 16, 1024, kSw128)
                                           : make_smem_desc(sbase + C::kA, 8192, 1024, kSw128);
             constexpr uint64_t kBStep = kBwd ? 2u : 128u;
+            const auto a_step = [](int ks) -> uint64_t { return (ks >> 2) * (16384u >> 4) + (ks & 3) * 2u; };
+            const auto b_step = [](int ks) -> uint64_t { return (ks >> 2) * (C::kBox >> 4) + (ks & 3) * kBStep; };
             bool ok = true;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const PairTile pt = pair_tile<BN>(tile, p);
@@ -215,14 +230,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t acc1 = tmem + b * C::kBufCols;
                 const uint32_t acc2 = acc1 + BN;
-                for (int kb = 0; kb < p.nkb; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb) {
                     if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
                     umma_bf16_pair(acc1, a_desc0 + so, b_desc0 + so, idesc, kb != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int ks = 1; ks < 4; ++ks)
-                        umma_bf16_pair(acc1, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc, 1u);
+                    for (int ks = 1; ks < 4 * kKB; ++ks)
+                        umma_bf16_pair(acc1, a_desc0 + so + a_step(ks), b_desc0 + so + b_step(ks), idesc, 1u);
                     umma_commit_pair(&empty[s], 3);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
@@ -232,14 +247,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
                     const int pass = t < tl.nb[0] ? 0 : 1;
                     const int tb = pass == 0 ? t : t - tl.nb[0];
-                    const int left = p.rt.ad[tl.a[pass]].rank - tb * 64;
-                    const int nks = left >= 64 ? 4 : (left + 15) / 16;
+                    const int left = p.rt.ad[tl.a[pass]].rank - tb * kBK;
+                    const int nks = left >= kBK ? 4 * kKB : (left + 15) / 16;
                     for (int ks = 0; ks < nks; ++ks) {
                         if (kBwd)
-                            umma_bf16_pair(acc2, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc,
+                            umma_bf16_pair(acc2, a_desc0 + so + a_step(ks), b_desc0 + so + b_step(ks), idesc,
                                            (t | ks) != 0 ? 1u : 0u);
                         else
-                            umma_bf16_pair(acc1, a_desc0 + so + 2 * ks, b_desc0 + so + kBStep * ks, idesc, 1u);
+                            umma_bf16_pair(acc1, a_desc0 + so + a_step(ks), b_desc0 + so + b_step(ks), idesc, 1u);
                     }
                     umma_commit_pair(&empty[s], 3);
                     if (++s == S) { s = 0; ph ^= 1u; }
