@@ -485,6 +485,85 @@ def timed_loop(fn, steps, stream, flush=None):
     return sum(a.elapsed_time(b) for a, b in pairs)
 
 
+def e2e_leg(prob_a, prob_b, wl, dev, stream, steps, barrier, max_over_ranks, ws_n):
+    """Steps through the public API with every step's inputs copied in from pinned host memory and its
+    results copied back, all inside the timed region.
+
+    Two buffer sets alternate between steps.  A host-to-device stream prefetches the inputs of step
+    i+1, and a device-to-host stream drains the outputs of step i-1, while step i computes on the
+    launch stream.  Events order each copy after the compute that frees its buffers.  A serial
+    variant (copy in, compute, copy out, one stream) is timed too.
+    """
+    import torch
+    sets = [prob_a, prob_b]
+    outs = [p.outputs() for p in sets]
+    hosts = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in o] for o in outs]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=False)  # noqa: E731
+    ev_in, ev_comp, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def copy_in(b):
+        with torch.cuda.stream(h2d_s):
+            for h, t in sets[b].inputs.values():
+                t.copy_(h, non_blocking=True)
+        ev_in[b].record(h2d_s)
+
+    def pipelined(n):
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        h2d_s.wait_event(start)
+        d2h_s.wait_event(start)
+        copy_in(0)
+        if n > 1:
+            copy_in(1)
+        for i in range(n):
+            b = i & 1
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_out[b])      # outputs of step i-2 are on the host
+            sets[b].step()
+            ev_comp[b].record(stream)
+            d2h_s.wait_event(ev_comp[b])
+            with torch.cuda.stream(d2h_s):
+                for h, t in zip(hosts[b], outs[b]):
+                    h.copy_(t, non_blocking=True)
+            ev_out[b].record(d2h_s)
+            if i + 2 < n:
+                h2d_s.wait_event(ev_comp[b])      # step i no longer reads buffer set b
+                copy_in(b)
+        stream.wait_event(ev_out[(n - 1) & 1])
+        if n > 1:
+            stream.wait_event(ev_out[n & 1])
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        return start.elapsed_time(end)
+
+    def serial():
+        for h, t in sets[0].inputs.values():
+            t.copy_(h, non_blocking=True)
+        sets[0].step()
+        for h, t in zip(hosts[0], outs[0]):
+            h.copy_(t, non_blocking=True)
+
+    pipelined(2)
+    serial()
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = max_over_ranks(pipelined(steps))
+    barrier()
+    ms_serial = max_over_ranks(timed_loop(serial, steps, stream))
+    for p in sets:
+        if p.status() != 0:
+            raise RuntimeError("a kernel reported a bounded-wait timeout in the end-to-end leg")
+    h2d = sum(h.numel() * h.element_size() for h, _ in sets[0].inputs.values())
+    d2h = sum(h.numel() * h.element_size() for h in hosts[0])
+    return {"value": wl.tokens * steps * ws_n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps, "steps": steps,
+            "overlap": "inputs of step i+1 and outputs of step i-1 copied on two copy streams while step i runs",
+            "serial_ms_per_step": ms_serial / steps,
+            "serial_value": wl.tokens * steps * ws_n / (ms_serial / 1e3)}
+
+
 def run_native(args):
     import torch
     import torch.distributed as dist
@@ -546,25 +625,8 @@ def run_native(args):
     # --- end to end through the public API with host buffers ---
     e2e = None
     if not args.no_e2e:
-        outs = prob.outputs()
-        hosts = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-        e2e_steps = max(3, min(args.steps, 20))
-
-        def e2e_step():
-            for h, t in prob.inputs.values():
-                t.copy_(h, non_blocking=True)
-            prob.step()
-            for h, t in zip(hosts, outs):
-                h.copy_(t, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        barrier()
-        e2e_ms = max_over_ranks(timed_loop(e2e_step, e2e_steps, stream))
-        h2d = sum(h.numel() * h.element_size() for h, _ in prob.inputs.values())
-        d2h = sum(h.numel() * h.element_size() for h in hosts)
-        e2e = {"value": wl.tokens * e2e_steps * ws_n / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / e2e_steps}
+        e2e = e2e_leg(prob, DeviceProblem(wl, dev, stream), wl, dev, stream, max(4, min(args.steps, 20)),
+                      barrier, max_over_ranks, ws_n)
 
     # --- frozen-layer reference points (overhead of the LoRA branch) ---
     frozen = None

@@ -338,7 +338,8 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         p.units = static_cast<int64_t>(c.rt.n_active) * p.nkb;
         p.seed_lo = seed_lo;
         p.seed_hi = seed_hi;
-        p.stages = kDownStages;
+        p.stage_bytes = 16384u + 128u * static_cast<uint32_t>(c.rt.rpad_max);
+        p.stages = static_cast<int32_t>(std::min<size_t>(12, kStageBudget / p.stage_bytes));
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
         LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));

@@ -19,8 +19,11 @@ namespace lora {
 
 namespace {
 
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 mask (2..5 also epilogue)
-constexpr int kMaskThreads = 256;
+constexpr int kMaskWarps = 8;                      // warps 2.. mask (2..5 also epilogue)
+constexpr int kMaskThreads = 32 * kMaskWarps;
+constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
+constexpr int kParts = kMaskThreads / 128;         // mask threads per token row
+constexpr int kChunks = 16 / kParts;               // 16-byte chunks (of the row's two boxes) per thread
 constexpr uint32_t kXBytes = 2u * 128u * 128u;   // 128 tokens x 128 features
 
 struct DaUnit {
@@ -153,12 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // warps 2..9 mask the two staged X boxes: thread -> (row, box) walks
-        // the 8 chunks of one row of one box.  Warps 2..5 also run the
-        // epilogue (TMEM lane quadrant = warp % 4).
+        // mask warps: thread -> (row, part) walks kChunks of the row's 16
+        // chunks (8 per 64-feature box).  Warps 2..5 also run the epilogue
+        // (TMEM lane quadrant = warp % 4).
         const int mt = threadIdx.x - 64;
         const int row = mt & 127;
-        const int h = mt >> 7;
+        const int part = mt >> 7;
         const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
@@ -172,13 +175,14 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (ad.T != 0u) {
-                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + h * 16384 + row * 128;
+                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
                 const uint32_t t = static_cast<uint32_t>(static_cast<int64_t>(d.tile) * kTileM + row);
-                const uint32_t g0 = static_cast<uint32_t>(d.fb * 16 + h * 8);
+                const uint32_t g0 = static_cast<uint32_t>(d.fb * 16);
 #pragma unroll
-                for (int c16 = 0; c16 < 8; ++c16) {
-                    const uint4 wv = philox_10(t, g0 + c16, keys);
-                    const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
+                for (int i = 0; i < kChunks; ++i) {
+                    const int cc = part * kChunks + i;          // chunk of the row: box cc / 8, chunk cc % 8
+                    const uint4 wv = philox_10(t, g0 + cc, keys);
+                    const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
                     uint4 v = lds128(addr);
                     v.x = apply_keep(v.x, wv.x, ad.T);
                     v.y = apply_keep(v.y, wv.y, ad.T);

@@ -23,17 +23,18 @@ namespace lora {
 
 namespace {
 
-constexpr int kThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2..9 mask (2..5 also epilogue)
-constexpr int kMaskThreads = 256;
-constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16
-constexpr uint32_t kABytes = 16384u;        // up to 64 rows x 128 bf16
-constexpr uint32_t kStageBytes = kXBytes + kABytes;
+constexpr int kMaskWarps = 8;                      // warps 2.. mask (2..5 also epilogue)
+constexpr int kMaskThreads = 32 * kMaskWarps;
+constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
+constexpr int kParts = kMaskThreads / 128;         // mask threads per tile row
+constexpr int kChunks = 8 / kParts;                // 16-byte chunks (8 features) per thread and stage
+constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16; then 64 rows of A (rpad_max x 2 bytes each)
 
 __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_constant__ DownParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
     uint64_t* full = bars;
     uint64_t* masked = bars + S;
     uint64_t* empty = bars + 2 * S;
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 const int a = p.rt.tile_adapter[tile];
                 const int rpad = p.rt.ad[a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
-                uint8_t* xs = smem + s * kStageBytes;
+                uint8_t* xs = smem + s * p.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], kXBytes + 128u * static_cast<uint32_t>(rpad));
                 tma_load_2d(xs, &p.mapX, &full[s], kb * 64, tile * kTileM);
                 tma_load_2d(xs + kXBytes, &p.mapA[a], &full[s], 0, kb * 64);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 if (!mbar_wait(&masked[s], ph, w, 3)) break;
                 tc_fence_after();
-                const uint32_t xs = smem_u32(smem + s * kStageBytes);
+                const uint32_t xs = smem_u32(smem + s * p.stage_bytes);
                 const uint32_t as = xs + kXBytes;
                 const uint32_t idesc = make_idesc_bf16(128, rpad, false, true);
                 const uint32_t sw = rank_swizzle(rpad);
@@ -149,13 +150,13 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // warps 2..9 mask the staged X tile: thread -> (row, half) covers the
-        // four 16-byte chunks [4*half, 4*half + 4) of one row, so the Philox
+        // mask warps: thread -> (row, part) covers the kChunks 16-byte chunks
+        // [kChunks*part, kChunks*part + kChunks) of one row, so the Philox
         // counter word is the row for all of them.  Warps 2..5 also run the
         // epilogue (TMEM lane quadrant = warp % 4).
         const int mt = threadIdx.x - 64;
         const int row = mt & 127;
-        const int half = mt >> 7;
+        const int part = mt >> 7;
         const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
@@ -172,16 +173,16 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (T != 0u || p.mask_bits != nullptr) {
-                const uint32_t xrow = smem_u32(smem + s * kStageBytes) + row * 128;
+                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
                 const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
-                uint4 wv[4];
+                uint4 wv[kChunks];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    wv[i] = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(kb * 8 + half * 4 + i), keys);
+                for (int i = 0; i < kChunks; ++i)
+                    wv[i] = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(kb * 8 + part * kChunks + i), keys);
                 if (T != 0u) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int c16 = half * 4 + i;
+                    for (int i = 0; i < kChunks; ++i) {
+                        const int c16 = part * kChunks + i;
                         const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
                         uint4 v = lds128(addr);
                         v.x = apply_keep(v.x, wv[i].x, T);
@@ -193,8 +194,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 if (p.mask_bits != nullptr && t < p.m) {
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int64_t g = static_cast<int64_t>(kb) * 8 + half * 4 + i;
+                    for (int i = 0; i < kChunks; ++i) {
+                        const int64_t g = static_cast<int64_t>(kb) * 8 + part * kChunks + i;
                         if (g * 8 < p.k) p.mask_bits[t * (p.k >> 3) + g] = static_cast<uint8_t>(keep_byte(wv[i], T));
                     }
                 }
@@ -256,15 +257,16 @@ __global__ void finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict_
 
 }  // namespace
 
-size_t down_smem_bytes(int stages) { return 1024 + stages * kStageBytes + (3 * stages + 5) * 8 + 16; }
+size_t down_smem_bytes(const DownParams& p) {
+    return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (3 * p.stages + 5) * 8 + 16;
+}
 
 cudaError_t down_configure() {
-    return cudaFuncSetAttribute(down_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(down_smem_bytes(kDownStages)));
+    return cudaFuncSetAttribute(down_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
-    down_proj_kernel<<<grid, kThreads, down_smem_bytes(p.stages), stream>>>(p);
+    down_proj_kernel<<<grid, kThreads, down_smem_bytes(p), stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -8,14 +8,13 @@
 
 namespace lora {
 
-constexpr int kDownStages = 6;
 // Dynamic shared memory a kernel may request; leaves room for its few bytes
 // of static shared memory under the 227 KB per-block limit.
 constexpr int kMaxDynSmem = 225 * 1024;
 // Stage ring budget of the rank-r kernels (stages * stage bytes).
 constexpr int kStageBudget = 220 * 1024;
 
-size_t down_smem_bytes(int stages);
+size_t down_smem_bytes(const DownParams& p);
 cudaError_t down_configure();
 cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream);

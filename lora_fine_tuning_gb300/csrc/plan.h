@@ -65,6 +65,7 @@ struct DownParams {
     int64_t units;                     // n_active * nkb
     uint32_t seed_lo, seed_hi;
     int32_t stages;
+    uint32_t stage_bytes;              // X tile (16 KB) + 64 rows of A (128 * rpad_max bytes)
 };
 
 // CTA-pair GEMM with the rank-r tail (k_gemm2.cu).
