@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDa << 8};
 
@@ -232,6 +234,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
 // dA_a = bf16(acc_a) (k x r_a), accumulators cleared; dSq rows of active tiles cleared.
 __global__ void finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
                                    int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     for (int a = 0; a < rt.n_adapters; ++a) {
@@ -278,13 +282,12 @@ cudaError_t da_configure() {
 }
 
 cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream) {
-    da_kernel<<<grid, kThreads, da_smem_bytes(p), stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(da_kernel, dim3(grid), dim3(kThreads), da_smem_bytes(p), stream, p);
 }
 
 cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream) {
-    finalize_da_kernel<<<2 * sms, 256, 0, stream>>>(p.acc_base, p.k, p.dsq, p.m, p.ld, p.rt, p.dA);
-    return cudaGetLastError();
+    return launch_pdl(finalize_da_kernel, dim3(2 * sms), dim3(256), 0, stream, p.acc_base, p.k, p.dsq, p.m, p.ld,
+                      p.rt, p.dA);
 }
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream) {

@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDown << 8};
 
@@ -243,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
 // r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.
 __global__ void finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
                                   const __grid_constant__ Routing rt) {
+    pdl_wait();
+    pdl_trigger();
     const int g8 = ld / 8;
     const int64_t total = m * g8;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -266,13 +270,11 @@ cudaError_t down_configure() {
 }
 
 cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
-    down_proj_kernel<<<grid, kThreads, down_smem_bytes(p), stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(down_proj_kernel, dim3(grid), dim3(kThreads), down_smem_bytes(p), stream, p);
 }
 
 cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream) {
-    finalize_s_kernel<<<2 * sms, 256, 0, stream>>>(p.S_acc, p.S_out, p.m, p.ld, p.rt);
-    return cudaGetLastError();
+    return launch_pdl(finalize_s_kernel, dim3(2 * sms), dim3(256), 0, stream, p.S_acc, p.S_out, p.m, p.ld, p.rt);
 }
 
 }  // namespace lora

@@ -68,6 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = *tmem_slot;
     const uint32_t tS = tmem;
     const uint32_t tB = tmem + static_cast<uint32_t>(rpad_max);
@@ -236,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
 __global__ void finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
                                      float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
                                      const __grid_constant__ AdapterPtrs dbp) {
+    pdl_wait();
+    pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     // dS: one thread per 8 columns of a row
@@ -295,13 +299,12 @@ cudaError_t dsdb_configure() {
 }
 
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
-    dsdb_kernel<<<grid, kThreads, dsdb_smem_bytes(p), stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(dsdb_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
 }
 
 cudaError_t launch_finalize_bwd1(const DsDbParams& p, int sms, cudaStream_t stream) {
-    finalize_bwd1_kernel<<<2 * sms, 256, 0, stream>>>(p.dS_acc, p.dSq, p.m, p.ld, p.acc_base, p.n, p.rt, p.dB);
-    return cudaGetLastError();
+    return launch_pdl(finalize_bwd1_kernel, dim3(2 * sms), dim3(256), 0, stream, p.dS_acc, p.dSq, p.m, p.ld,
+                      p.acc_base, p.n, p.rt, p.dB);
 }
 
 }  // namespace lora

@@ -132,6 +132,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, (kBwd ? kKGemmBwd : kKGemmFwd) << 8};
 
@@ -397,14 +399,9 @@ cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStr
     if (pairs > sms / 2) pairs = sms / 2;
     if (pairs < 1) pairs = 1;
     const dim3 grid(2 * pairs);
-    if (!bwd) {
-        gemm2_kernel<false, 256><<<grid, kThreads, smem_bytes<false, 256>(), stream>>>(p);
-    } else if (bn == 128) {
-        gemm2_kernel<true, 128><<<grid, kThreads, smem_bytes<true, 128>(), stream>>>(p);
-    } else {
-        gemm2_kernel<true, 256><<<grid, kThreads, smem_bytes<true, 256>(), stream>>>(p);
-    }
-    return cudaGetLastError();
+    if (!bwd) return launch_pdl(gemm2_kernel<false, 256>, grid, dim3(kThreads), smem_bytes<false, 256>(), stream, p);
+    if (bn == 128) return launch_pdl(gemm2_kernel<true, 128>, grid, dim3(kThreads), smem_bytes<true, 128>(), stream, p);
+    return launch_pdl(gemm2_kernel<true, 256>, grid, dim3(kThreads), smem_bytes<true, 256>(), stream, p);
 }
 
 }  // namespace lora

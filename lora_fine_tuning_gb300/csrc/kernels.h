@@ -2,11 +2,31 @@
 #pragma once
 
 #include <cstddef>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "plan.h"
 
 namespace lora {
+
+// Launches a kernel on `stream` with programmatic stream serialization: it may
+// start while the previous kernel on the stream finishes, and waits for it with
+// griddepcontrol.wait before touching global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Dynamic shared memory a kernel may request; leaves room for its few bytes
 // of static shared memory under the 227 KB per-block limit.
