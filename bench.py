@@ -223,7 +223,7 @@ def dist_env():
 
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while running."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -236,7 +236,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -249,6 +249,10 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
+    def mark(self, what: str):
+        """Wall-clock bounds of the timed region: samples outside them are not summarised."""
+        setattr(self, what, time.time())
+
     def __exit__(self, *exc):
         if self.proc is not None:
             time.sleep(0.2)
@@ -260,26 +264,33 @@ class ClockSampler:
         return False
 
     def summary(self):
-        sm, mx, pw, reasons = [], [], [], set()
+        import datetime
+        t0, t1 = getattr(self, "start", None), getattr(self, "stop", None)
+        sm, mx, pw, reasons, inside = [], [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-                pw.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                vals = (float(parts[1]), float(parts[2]), float(parts[3]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[4:8]):
+            if t0 is not None and t1 is not None and not (t0 - 0.025 <= ts <= t1 + 0.025):
+                continue
+            inside += 1
+            sm.append(vals[0])
+            mx.append(vals[1])
+            pw.append(vals[2])
+            for name, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        loaded = [s for s, p in zip(sm, pw) if p > 0.5 * max(pw)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(pw)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no nvidia-smi sample fell inside the timed region"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": inside, "power_w_max": max(pw), "sampling": "nvidia-smi every 20 ms, timed region only"}
 
 
 def source_digest(files):
@@ -610,7 +621,9 @@ def run_native(args):
     with ClockSampler(local) as clocks:
         barrier()
         torch.cuda.synchronize(dev)
+        clocks.mark("start")
         elapsed_ms = timed_loop(prob.step, args.steps, stream, flush)
+        clocks.mark("stop")
         barrier()
     elapsed_ms = max_over_ranks(elapsed_ms)
     clk = clocks.summary()
@@ -707,7 +720,7 @@ def run_native(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, LAYER])
