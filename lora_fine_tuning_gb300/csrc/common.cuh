@@ -329,6 +329,32 @@ __device__ __forceinline__ uint32_t apply_keep(uint32_t data, uint32_t w, uint32
     return data;
 }
 
+// Walks units u = slot * nblk + blk (slot: an active tile, blk: a block of the
+// other dimension) from u0 on, in order, without a division per unit; the
+// slot's tile and adapter are looked up once per slot.  Every role of a kernel
+// walks the same sequence with its own copy.
+struct TileBlockIter {
+    int slot, blk, nblk, tile, a;
+    __device__ __forceinline__ TileBlockIter(int64_t u0, int nblk_, const Routing& rt) : nblk(nblk_) {
+        slot = static_cast<int>(u0 / nblk_);
+        blk = static_cast<int>(u0 - static_cast<int64_t>(slot) * nblk_);
+        load(rt);
+    }
+    __device__ __forceinline__ void load(const Routing& rt) {
+        if (slot < rt.n_active) {
+            tile = rt.active_tiles[slot];
+            a = rt.tile_adapter[tile];
+        }
+    }
+    __device__ __forceinline__ void next(const Routing& rt) {
+        if (++blk == nblk) {
+            blk = 0;
+            ++slot;
+            load(rt);
+        }
+    }
+};
+
 // Eight keep bits (bit e = element e of the 8-group).
 __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
     uint32_t b = 0;

@@ -44,6 +44,23 @@ __device__ __forceinline__ DaUnit da_unit(int64_t u, const DaParams& p) {
     return d;
 }
 
+// The unit after d in the order of da_unit (tile fastest, then feature block,
+// then adapter), without a division; adapters without tiles have no units.
+__device__ __forceinline__ void da_next(DaUnit& d, const DaParams& p) {
+    if (++d.ti == d.n_a) {
+        d.ti = 0;
+        if (++d.fb == p.nfb) {
+            d.fb = 0;
+            do {
+                ++d.a;
+            } while (d.a < p.rt.n_adapters && p.rt.adapter_begin[d.a + 1] == p.rt.adapter_begin[d.a]);
+            if (d.a >= p.rt.n_adapters) return;   // past the last unit
+            d.n_a = p.rt.adapter_begin[d.a + 1] - p.rt.adapter_begin[d.a];
+        }
+    }
+    d.tile = p.rt.active_tiles[p.rt.adapter_begin[d.a] + d.ti];
+}
+
 __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__ DaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -100,8 +117,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t u = u0; u < u1; ++u) {
-                const DaUnit d = da_unit(u, p);
+            DaUnit d = da_unit(u0, p);
+            for (int64_t u = u0; u < u1; ++u, da_next(d, p)) {
                 const int rpad = p.rt.ad[d.a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                 uint8_t* st = smem + s * p.stage_bytes;
@@ -124,9 +141,22 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             int s = 0;
             uint32_t ph = 0;
             uint32_t use = 0;
-            for (int64_t u = u0; u < u1; ++u) {
-                const DaUnit d = da_unit(u, p);
+            // Operand descriptors of stage 0, built once (dSq's when the padded rank
+            // changes); an MMA only moves the start-address field (bytes / 16).
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t x_d0 = make_smem_desc(sbase, 16384, 1024, kSw128);   // X^T, MN-major (two 64-wide atoms)
+            int cur_rpad = -1;
+            uint32_t idesc = 0, rb = 0;
+            uint64_t d_d0 = 0;
+            DaUnit d = da_unit(u0, p);
+            for (int64_t u = u0; u < u1; ++u, da_next(d, p)) {
                 const int rpad = p.rt.ad[d.a].rpad;
+                if (rpad != cur_rpad) {
+                    cur_rpad = rpad;
+                    idesc = make_idesc_bf16(128, rpad, true, true);
+                    rb = rank_row_bytes(rpad);
+                    d_d0 = make_smem_desc(sbase + p.off_d, 16384, 8u * rb, rank_swizzle(rpad));   // dSq, MN-major
+                }
                 const bool first = (u == u0) || d.ti == 0;
                 const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
                 const uint32_t b = use & 1u;
@@ -136,17 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 if (!mbar_wait(&masked[s], ph, w, 3)) break;
                 tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
-                const uint32_t idesc = make_idesc_bf16(128, rpad, true, true);
-                const uint32_t sw = rank_swizzle(rpad);
-                const uint32_t rb = rank_row_bytes(rpad);
+                const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
                 const uint32_t dacc = tmem + b * static_cast<uint32_t>(rpad_max);
+                // 16 tokens per step: 2048 B of X (16 rows of 128 B), 16 * rb B of dSq
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = make_smem_desc(st + ks * 2048u, 16384, 1024, kSw128);
-                    const uint64_t bd = make_smem_desc(st + p.off_d + ks * 16u * rb, 16384, 8u * rb, sw);
-                    umma_bf16(dacc, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(dacc, x_d0 + so + ks * 128u, d_d0 + so + static_cast<uint64_t>(ks) * rb, idesc,
+                              (first && ks == 0) ? 0u : 1u);
                 umma_commit(&empty[s]);
                 if (last) {
                     umma_commit(&acc_full[b]);
@@ -170,8 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const DaUnit d = da_unit(u, p);
+        DaUnit d = da_unit(u0, p);
+        for (int64_t u = u0; u < u1; ++u, da_next(d, p)) {
             const AdapterDev ad = p.rt.ad[d.a];
             const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
             bool ok = mbar_wait(&full[s], ph, w, 4);

@@ -86,11 +86,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t u = u0; u < u1; ++u) {
-                const int slot = static_cast<int>(u / p.nkb);
-                const int kb = static_cast<int>(u % p.nkb);
-                const int tile = p.rt.active_tiles[slot];
-                const int a = p.rt.tile_adapter[tile];
+            TileBlockIter it(u0, p.nkb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int kb = it.blk;
+                const int tile = it.tile;
+                const int a = it.a;
                 const int rpad = p.rt.ad[a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                 uint8_t* xs = smem + s * p.stage_bytes;
@@ -113,12 +113,23 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             int s = 0;
             uint32_t ph = 0;
             uint32_t use = 0;
-            for (int64_t u = u0; u < u1; ++u) {
-                const int slot = static_cast<int>(u / p.nkb);
-                const int kb = static_cast<int>(u % p.nkb);
-                const int tile = p.rt.active_tiles[slot];
-                const int a = p.rt.tile_adapter[tile];
-                const int rpad = p.rt.ad[a].rpad;
+            // Operand descriptors of stage 0, built once (the A_a block's when the padded
+            // rank changes); an MMA only moves the start-address field (bytes / 16).
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t x_d0 = make_smem_desc(sbase, 16, 1024, kSw128);   // X tile, K-major
+            int cur_rpad = -1;
+            uint32_t idesc = 0, rb = 0;
+            uint64_t a_d0 = 0;
+            TileBlockIter it(u0, p.nkb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int kb = it.blk;
+                const int rpad = p.rt.ad[it.a].rpad;
+                if (rpad != cur_rpad) {
+                    cur_rpad = rpad;
+                    idesc = make_idesc_bf16(128, rpad, false, true);
+                    rb = rank_row_bytes(rpad);
+                    a_d0 = make_smem_desc(sbase + kXBytes, 8192, 8 * rb, rank_swizzle(rpad));   // A_a rows, MN-major
+                }
                 const bool first = (u == u0) || kb == 0;
                 const bool last = (u == u1 - 1) || kb == p.nkb - 1;
                 const uint32_t b = use & 1u;
@@ -128,18 +139,13 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 if (!mbar_wait(&masked[s], ph, w, 3)) break;
                 tc_fence_after();
-                const uint32_t xs = smem_u32(smem + s * p.stage_bytes);
-                const uint32_t as = xs + kXBytes;
-                const uint32_t idesc = make_idesc_bf16(128, rpad, false, true);
-                const uint32_t sw = rank_swizzle(rpad);
-                const uint32_t rb = rank_row_bytes(rpad);
+                const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
                 const uint32_t d = tmem + b * static_cast<uint32_t>(rpad_max);
+                // 16 features per step: 32 B of the X row, 16 rows (16 * rb B) of A_a
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint64_t ad = make_smem_desc(xs + ks * 32, 16, 1024, kSw128);
-                    const uint64_t bd = make_smem_desc(as + ks * 16 * rb, 8192, 8 * rb, sw);
-                    umma_bf16(d, ad, bd, idesc, (first && ks == 0) ? 0u : 1u);
-                }
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(d, x_d0 + so + ks * 2u, a_d0 + so + static_cast<uint64_t>(ks) * rb, idesc,
+                              (first && ks == 0) ? 0u : 1u);
                 umma_commit(&empty[s]);
                 if (last) {
                     umma_commit(&acc_full[b]);
@@ -165,11 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int slot = static_cast<int>(u / p.nkb);
-            const int kb = static_cast<int>(u % p.nkb);
-            const int tile = p.rt.active_tiles[slot];
-            const int a = p.rt.tile_adapter[tile];
+        TileBlockIter it(u0, p.nkb, p.rt);
+        for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+            const int kb = it.blk;
+            const int tile = it.tile;
+            const int a = it.a;
             const uint32_t T = p.rt.ad[a].T;
             const bool last = (u == u1 - 1) || kb == p.nkb - 1;
             bool ok = mbar_wait(&full[s], ph, w, 4);

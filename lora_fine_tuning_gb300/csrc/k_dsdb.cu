@@ -86,11 +86,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t u = u0; u < u1; ++u) {
-                const int slot = static_cast<int>(u / p.nnb);
-                const int nb = static_cast<int>(u % p.nnb);
-                const int tile = p.rt.active_tiles[slot];
-                const int a = p.rt.tile_adapter[tile];
+            TileBlockIter it(u0, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int nb = it.blk;
+                const int tile = it.tile;
+                const int a = it.a;
                 const int rpad = p.rt.ad[a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                 uint8_t* st = smem + s * p.stage_bytes;
@@ -115,12 +115,28 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
             int s = 0;
             uint32_t ph = 0;
             uint32_t units_done = 0, items_done = 0;
-            for (int64_t u = u0; u < u1; ++u) {
-                const int slot = static_cast<int>(u / p.nnb);
-                const int nb = static_cast<int>(u % p.nnb);
-                const int tile = p.rt.active_tiles[slot];
-                const int a = p.rt.tile_adapter[tile];
-                const int rpad = p.rt.ad[a].rpad;
+            // Operand descriptors of stage 0, built once: an MMA only moves the start-address
+            // field (bytes / 16) by its stage and K step.  The rank-dependent ones (N = rpad,
+            // S' layout) are rebuilt when the adapter's padded rank changes.
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t ds_a0 = make_smem_desc(sbase, 16, 1024, kSw128);              // dY, K-major
+            const uint64_t ds_b0 = make_smem_desc(sbase + p.off_b, 16, 1024, kSw128);    // B_a, K-major
+            const uint64_t db_a0 = make_smem_desc(sbase, 16384, 1024, kSw128);           // dY^T, MN-major
+            const uint32_t bbox16 = bbox >> 4;
+            int cur_rpad = -1;
+            uint32_t idesc_s = 0, idesc_b = 0, rb = 0;
+            uint64_t db_b0 = 0;
+            TileBlockIter it(u0, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int nb = it.blk;
+                const int rpad = p.rt.ad[it.a].rpad;
+                if (rpad != cur_rpad) {
+                    cur_rpad = rpad;
+                    idesc_s = make_idesc_bf16(128, rpad, false, false);
+                    idesc_b = make_idesc_bf16(128, rpad, true, true);
+                    rb = rank_row_bytes(rpad);
+                    db_b0 = make_smem_desc(sbase + p.off_s, 16384, 8u * rb, rank_swizzle(rpad));   // S', MN-major
+                }
                 const bool first = (u == u0) || nb == 0;
                 const bool last = (u == u1 - 1) || nb == p.nnb - 1;
                 if (first) {
@@ -132,26 +148,21 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
                 tc_fence_after();
                 if (!mbar_wait(&full[s], ph, w, 4)) break;
                 tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * p.stage_bytes);
-                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad)
-                const uint32_t idesc_s = make_idesc_bf16(128, rpad, false, false);
+                const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
+                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t h = static_cast<uint32_t>(ks >> 2), kk = static_cast<uint32_t>(ks & 3);
-                    const uint64_t ad = make_smem_desc(st + h * 16384u + kk * 32u, 16, 1024, kSw128);
-                    const uint64_t bd = make_smem_desc(st + p.off_b + h * bbox + kk * 32u, 16, 1024, kSw128);
-                    umma_bf16(tS, ad, bd, idesc_s, (first && ks == 0) ? 0u : 1u);
+                    const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
+                    umma_bf16(tS, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
+                              (first && ks == 0) ? 0u : 1u);
                 }
-                // dB^T = dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens, N = rpad)
-                const uint32_t idesc_b = make_idesc_bf16(128, rpad, true, true);
-                const uint32_t sw = rank_swizzle(rpad);
-                const uint32_t rb = rank_row_bytes(rpad);
+                // dB^T = dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens, N = rpad):
+                // 16 tokens per step = 2048 B of dY and 16 * rb B of S'
+                const uint32_t dB_acc = tB + bb * static_cast<uint32_t>(rpad_max);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t ad = make_smem_desc(st + ks * 2048u, 16384, 1024, kSw128);
-                    const uint64_t bd = make_smem_desc(st + p.off_s + ks * 16u * rb, 16384, 8u * rb, sw);
-                    umma_bf16(tB + bb * static_cast<uint32_t>(rpad_max), ad, bd, idesc_b, ks != 0 ? 1u : 0u);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
+                              ks != 0 ? 1u : 0u);
                 umma_commit(&empty[s]);
                 umma_commit(&accB_full[bb]);
                 ++units_done;
@@ -168,12 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t units_done = 0, items_done = 0;
-        for (int64_t u = u0; u < u1; ++u) {
-            const int slot = static_cast<int>(u / p.nnb);
-            const int nb = static_cast<int>(u % p.nnb);
-            const int tile = p.rt.active_tiles[slot];
-            const int a = p.rt.tile_adapter[tile];
-            const AdapterDev ad = p.rt.ad[a];
+        TileBlockIter it(u0, p.nnb, p.rt);
+        for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+            const int nb = it.blk;
+            const int tile = it.tile;
+            const AdapterDev ad = p.rt.ad[it.a];
             const bool last = (u == u1 - 1) || nb == p.nnb - 1;
             const uint32_t bb = units_done & 1u;
             bool ok = mbar_wait(&accB_full[bb], (units_done >> 1) & 1u, w, 5);
