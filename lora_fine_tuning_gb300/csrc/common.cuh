@@ -313,6 +313,76 @@ __device__ __forceinline__ uint4 philox_10(uint32_t c0, uint32_t c1, uint32_t k0
     return philox_10(c0, c1, philox_keys(k0, k1));
 }
 
+// The same generator for many counters (t, c1) of one row t.  With x2 = x3 = 0
+// at the start, the words that rounds 1-3 compute from t alone are the same for
+// every c1; they are computed once per row here, and philox_10_row finishes the
+// rest (two products and four XORs fewer per call than philox_10).
+struct PhiloxRow {
+    uint32_t a2, b3, c0, d1k, e2, f3;   // round 1: x2, x3; round 2: x0, x1 ^ k0[2]; round 3: x2 part, x3
+};
+
+__device__ __forceinline__ PhiloxRow philox_row(uint32_t t, const PhiloxKeys& K) {
+    PhiloxRow R;
+    const uint64_t p0 = static_cast<uint64_t>(t) * 0xD2511F53u;              // round 1: x0 * M0
+    R.a2 = static_cast<uint32_t>(p0 >> 32) ^ K.k1[0];                        // round 1: x2
+    R.b3 = static_cast<uint32_t>(p0);                                         // round 1: x3
+    const uint64_t p1 = static_cast<uint64_t>(R.a2) * 0xCD9E8D57u;           // round 2: x2 * M1
+    R.c0 = static_cast<uint32_t>(p1 >> 32) ^ K.k0[1];                        // round 2: x0 (x1 was 0)
+    R.d1k = static_cast<uint32_t>(p1) ^ K.k0[2];                             // round 2: x1, with round 3's key
+    const uint64_t q0 = static_cast<uint64_t>(R.c0) * 0xD2511F53u;           // round 3: x0 * M0
+    R.e2 = static_cast<uint32_t>(q0 >> 32) ^ K.k1[2];                        // round 3: x2 = this ^ x3
+    R.f3 = static_cast<uint32_t>(q0);                                         // round 3: x3
+    return R;
+}
+
+__device__ __forceinline__ uint4 philox_10_row(const PhiloxRow& R, uint32_t c1, const PhiloxKeys& K) {
+    // round 1: x0 = c1 ^ k0[0], x1 = 0, x2 = a2, x3 = b3
+    const uint32_t y0 = c1 ^ K.k0[0];
+    // round 2: x2 = hi(y0 * M0) ^ b3 ^ k1[1], x3 = lo(y0 * M0); x0, x1 per row
+    const uint64_t p0 = static_cast<uint64_t>(y0) * 0xD2511F53u;
+    const uint32_t z2 = static_cast<uint32_t>(p0 >> 32) ^ R.b3 ^ K.k1[1];
+    const uint32_t z3 = static_cast<uint32_t>(p0);
+    // round 3: x0 = hi(z2 * M1) ^ x1 ^ k0[2], x1 = lo(z2 * M1), x2 = e2 ^ z3, x3 = f3
+    const uint64_t p1 = static_cast<uint64_t>(z2) * 0xCD9E8D57u;
+    uint32_t x0 = static_cast<uint32_t>(p1 >> 32) ^ R.d1k;
+    uint32_t x1 = static_cast<uint32_t>(p1);
+    uint32_t x2 = R.e2 ^ z3;
+    uint32_t x3 = R.f3;
+#pragma unroll
+    for (int r = 3; r < 10; ++r) {
+        const uint64_t q0 = static_cast<uint64_t>(x0) * 0xD2511F53u;
+        const uint64_t q1 = static_cast<uint64_t>(x2) * 0xCD9E8D57u;
+        x0 = static_cast<uint32_t>(q1 >> 32) ^ x1 ^ K.k0[r];
+        x1 = static_cast<uint32_t>(q1);
+        x2 = static_cast<uint32_t>(q0 >> 32) ^ x3 ^ K.k1[r];
+        x3 = static_cast<uint32_t>(q0);
+    }
+    return make_uint4(x0, x1, x2, x3);
+}
+
+// Constants of the keep test lane >= T (0 < T <= 65536) written as a carry:
+// lane + (65536 - T) carries out of the lane's 16 bits exactly when it keeps.
+struct KeepTest {
+    uint32_t low, top;   // low 15 bits and top bit of 65536 - T, in both 16-bit lanes
+};
+
+__device__ __forceinline__ KeepTest keep_test(uint32_t T) {
+    const uint32_t c = 65536u - T;
+    return KeepTest{(c & 0x7FFFu) * 0x10001u, (c & 0x8000u) * 0x10001u};
+}
+
+// Zeroes the dropped elements of a packed bf16 pair: the low 15 bits of both
+// lanes are added without crossing lanes, the carry out of each lane is the
+// majority of its top bits and the carry into them, and a byte permute spreads
+// each carry (bits 15, 31) over its lane.
+__device__ __forceinline__ uint32_t apply_keep_fast(uint32_t data, uint32_t w, const KeepTest& kt) {
+    const uint32_t s = (w & 0x7FFF7FFFu) + kt.low;
+    const uint32_t carry = (w & kt.top) | (w & s) | (kt.top & s);
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(carry));
+    return data & m;
+}
+
 // One Philox word covers two bf16 elements: the low 16-bit lane decides the
 // element in the low half of a packed pair, the high lane the high half.
 // Returns an AND mask that keeps the element bits where lane >= T.

@@ -193,6 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
         const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
+        uint32_t prow_t = 0xFFFFFFFFu;   // row whose Philox words are in prow
+        PhiloxRow prow{};
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
@@ -206,16 +208,21 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
                 const uint32_t t = static_cast<uint32_t>(static_cast<int64_t>(d.tile) * kTileM + row);
                 const uint32_t g0 = static_cast<uint32_t>(d.fb * 16);
+                if (t != prow_t) {
+                    prow_t = t;
+                    prow = philox_row(t, keys);
+                }
+                const KeepTest kt = keep_test(ad.T);
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i) {
                     const int cc = part * kChunks + i;          // chunk of the row: box cc / 8, chunk cc % 8
-                    const uint4 wv = philox_10(t, g0 + cc, keys);
+                    const uint4 wv = philox_10_row(prow, g0 + cc, keys);
                     const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
                     uint4 v = lds128(addr);
-                    v.x = apply_keep(v.x, wv.x, ad.T);
-                    v.y = apply_keep(v.y, wv.y, ad.T);
-                    v.z = apply_keep(v.z, wv.z, ad.T);
-                    v.w = apply_keep(v.w, wv.w, ad.T);
+                    v.x = apply_keep_fast(v.x, wv.x, kt);
+                    v.y = apply_keep_fast(v.y, wv.y, kt);
+                    v.z = apply_keep_fast(v.z, wv.z, kt);
+                    v.w = apply_keep_fast(v.w, wv.w, kt);
                     sts128(addr, v);
                 }
             }

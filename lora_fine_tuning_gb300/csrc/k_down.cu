@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
         const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
+        uint32_t prow_t = 0xFFFFFFFFu;   // row whose Philox words are in prow
+        PhiloxRow prow{};
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
@@ -183,20 +185,25 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             if (T != 0u || p.mask_bits != nullptr) {
                 const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
                 const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
+                if (static_cast<uint32_t>(t) != prow_t) {
+                    prow_t = static_cast<uint32_t>(t);
+                    prow = philox_row(prow_t, keys);
+                }
                 uint4 wv[kChunks];
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i)
-                    wv[i] = philox_10(static_cast<uint32_t>(t), static_cast<uint32_t>(kb * 8 + part * kChunks + i), keys);
+                    wv[i] = philox_10_row(prow, static_cast<uint32_t>(kb * 8 + part * kChunks + i), keys);
                 if (T != 0u) {
+                    const KeepTest kt = keep_test(T);
 #pragma unroll
                     for (int i = 0; i < kChunks; ++i) {
                         const int c16 = part * kChunks + i;
                         const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
                         uint4 v = lds128(addr);
-                        v.x = apply_keep(v.x, wv[i].x, T);
-                        v.y = apply_keep(v.y, wv[i].y, T);
-                        v.z = apply_keep(v.z, wv[i].z, T);
-                        v.w = apply_keep(v.w, wv[i].w, T);
+                        v.x = apply_keep_fast(v.x, wv[i].x, kt);
+                        v.y = apply_keep_fast(v.y, wv[i].y, kt);
+                        v.z = apply_keep_fast(v.z, wv[i].z, kt);
+                        v.w = apply_keep_fast(v.w, wv[i].w, kt);
                         sts128(addr, v);
                     }
                 }
