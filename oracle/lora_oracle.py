@@ -318,3 +318,60 @@ def multi_lora_backward(dY, X, W, adapters, segments, seed: int, rows=None):
         dB_list.append(dBi)
         dS_list.append(dSi)
     return dX, dA_list, dB_list, dS_list, owner
+
+
+# ---------------------------------------------------------------------------
+# Greedy token-capacity packing of samples into microbatches
+# ---------------------------------------------------------------------------
+#
+# The multi-adapter scheduler (LoRAFusion notes, papers.chlience.com, section 5
+# "Multi-LoRA scheduler"; the article, juhe.plus, section 4.2 step 2) packs the
+# samples of a group into microbatches that each hold at most a token capacity,
+# solving a two-stage MILP and falling back to greedy packing when the solver
+# times out.  The pages do not spell the greedy algorithm out; the reading taken
+# here is the textbook greedy for bin packing, first-fit decreasing.  A sample
+# occupies its length rounded up to whole 128-row tiles, because the
+# multi-adapter kernels route whole tiles.
+
+
+def padded_rows(length: int) -> int:
+    """Rows a sample of `length` tokens occupies: whole 128-row tiles."""
+    return -(-int(length) // TILE_ROWS) * TILE_ROWS
+
+
+def greedy_pack(lengths, capacity: int):
+    """First-fit decreasing packing.  Returns (batch_of_sample, row_of_sample, n_batches).
+
+    Samples are taken in order of decreasing padded size (equal sizes: lower
+    sample index first).  Each goes into the first microbatch, in the order the
+    microbatches were opened, whose remaining rows can hold it; if none can, a
+    new microbatch is opened.  Inside a microbatch the samples lie one after
+    another in the order they were placed, so row_of_sample is where the sample
+    starts.  Raises ValueError for a sample longer than the capacity, a length
+    below 1, or a capacity that is not a positive multiple of 128.
+    """
+    if capacity <= 0 or capacity % TILE_ROWS:
+        raise ValueError("capacity must be a positive multiple of 128 rows")
+    sizes = []
+    for length in lengths:
+        if int(length) < 1:
+            raise ValueError("sample lengths must be at least 1")
+        size = padded_rows(length)
+        if size > capacity:
+            raise ValueError("a sample does not fit in one microbatch")
+        sizes.append(size)
+    order = sorted(range(len(sizes)), key=lambda i: (-sizes[i], i))
+    used = []                                   # rows filled in each open microbatch
+    batch = [0] * len(sizes)
+    row = [0] * len(sizes)
+    for i in order:
+        for b, filled in enumerate(used):
+            if filled + sizes[i] <= capacity:
+                break
+        else:
+            b = len(used)
+            used.append(0)
+        batch[i] = b
+        row[i] = used[b]
+        used[b] += sizes[i]
+    return batch, row, len(used)
