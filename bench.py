@@ -51,6 +51,7 @@ def load_peaks():
 
 
 MULTI = "multi_4ad"      # packed batch, four adapters with ranks 16/16/32/64 on one 8192x8192 weight
+GREEDY = "multi_4ad_greedy"   # a global batch of the same samples packed into 16384-row microbatches (greedy)
 LAYER = "llama8b_layer"  # the seven LoRA projections of one Llama-3.1-8B decoder layer
 
 
@@ -78,9 +79,40 @@ class Workload:
     layer runs its seven linears forward in order, then backward in reverse.
     """
 
-    def __init__(self, name: str, m=None, r=None):
+    def __init__(self, name: str, m=None, r=None, packer=None):
         self.name = name
-        if name == MULTI:
+        if name == GREEDY:
+            # samples for four microbatches' worth of rows, packed first-fit decreasing into microbatches
+            # of 16384 rows; one multi-adapter call per microbatch, all on the same layer
+            w = synth.MULTI_WORKLOAD
+            specs = [(s.rank, s.alpha, s.p) for s in w["specs"]]
+            cap = m or w["total_rows"]
+            lengths, ads = synth.sample_stream(w["seed"], 4 * cap, len(specs))
+            batches = packer(lengths, ads, cap)
+            self.m = cap
+            base = synth.multi_inputs(w["seed"], w["k"], w["n"], w["specs"], synth.PackedBatch(m=128))
+            self.parts, owners, valid_rows = [], [], []
+            for b, mb in enumerate(batches):
+                pb = synth.PackedBatch(m=cap, segments=mb["segments"], valid=mb["valid"])
+                raw = synth.multi_inputs(w["seed"] + 1000 + b, w["k"], w["n"], w["specs"], pb)
+                self.parts.append(Part(f"microbatch{b}", w["k"], w["n"], specs, w["seed"] + b, raw["X"], base["W"],
+                                       raw["dY"], base["adapters"], list(mb["segments"]), x_key=f"X{b}"))
+            self.n_samples = len(lengths)
+            self.n_batches = len(batches)
+            self.packed_rows = sum(mb["rows"] for mb in batches)
+            self.valid_tokens = int(sum(lengths))
+            self.token_count = [(i, lengths[i]) for i in range(len(lengths))]
+            self.owner = None
+            self.valid_rows = np.arange(self.valid_tokens)   # counts only; per-part rows are in the parts
+            self.spec_tokens = [sum(l for l, a in zip(lengths, ads) if a == i) for i in range(len(specs))]
+            # the CPU legs run the oracle on rows of the first microbatch
+            mb0 = batches[0]
+            self.cpu_parts = self.parts[:1]
+            self.row_pool = np.concatenate([np.arange(st, st + v) for (st, _r, _a), v in zip(mb0["segments"],
+                                                                                               mb0["valid"])])
+            self.spec_rows = [sum(-(-l // 128) * 128 for l, a in zip(lengths, ads) if a == i)
+                              for i in range(len(specs))]
+        elif name == MULTI:
             w = synth.MULTI_WORKLOAD
             specs = [(s.rank, s.alpha, s.p) for s in w["specs"]]
             batch = synth.packed_batch(w["seed"], m or w["total_rows"], len(specs))
@@ -122,14 +154,29 @@ class Workload:
     def tokens(self) -> int:
         return int(self.valid_rows.size)
 
+    @property
+    def sample_pool(self):
+        """Global rows the CPU legs sample from."""
+        return getattr(self, "row_pool", self.valid_rows)
+
     def tokens_of(self, i: int) -> int:
+        if self.name == GREEDY:
+            return self.spec_tokens[i]
         return int(np.count_nonzero(self.owner[self.valid_rows] == i))
 
     def rows_of(self, i: int) -> int:
         """Rows (padding included) the kernels run adapter i on."""
+        if self.name == GREEDY:
+            return self.spec_rows[i]
         return int(np.count_nonzero(self.owner == i))
 
     def describe(self) -> str:
+        if self.name == GREEDY:
+            q = self.parts[0]
+            ads = ", ".join(f"(r={r}, alpha={a}, p={p})" for r, a, p in q.specs)
+            return (f"{self.name}: {self.n_samples} samples (lognormal lengths, {self.valid_tokens} tokens) packed "
+                    f"first-fit decreasing into {self.n_batches} microbatches of {self.m} rows "
+                    f"({self.packed_rows} rows used by tiles), k={q.k}, n={q.n}, adapters {ads}")
         if self.name == MULTI:
             q = self.parts[0]
             ads = ", ".join(f"(r={r}, alpha={a}, p={p})" for r, a, p in q.specs)
@@ -147,9 +194,9 @@ class Workload:
 
     def layer_flops(self) -> int:
         """Algorithmic FLOPs of one fwd+bwd over the valid tokens: per linear 4Tkn + sum_i 6 T_i r_i (k+n)
-        (W is frozen: no weight gradient)."""
+        (W is frozen: no weight gradient).  Microbatches of one layer count as one linear."""
         F = 0
-        for q in self.parts:
+        for q in (self.parts[:1] if self.name == GREEDY else self.parts):
             F += 4 * self.tokens * q.k * q.n
             F += sum(6 * self.tokens_of(i) * r * (q.k + q.n) for i, (r, _, _) in enumerate(q.specs))
         return F
@@ -162,7 +209,7 @@ class Workload:
         """
         T = self.tokens
         total = 0
-        for q in self.parts:
+        for q in (self.parts[:1] if self.name == GREEDY else self.parts):
             k, n = q.k, q.n
             fwd = T * k + k * n + T * n
             bwd = T * n + k * n + 2 * T * k
@@ -179,9 +226,11 @@ class Workload:
         if kind not in ("gemm_fwd", "gemm_bwd"):
             return None
         F = 0
-        for q in self.parts:
+        for j, q in enumerate(self.parts):
             out = q.n if kind == "gemm_fwd" else q.k
-            F += 2 * self.m * q.k * q.n + sum(2 * self.rows_of(i) * r * out for i, (r, _, _) in enumerate(q.specs))
+            F += 2 * self.m * q.k * q.n
+            if self.name != GREEDY or j == 0:   # a packed global batch: the tails of all its rows, once
+                F += sum(2 * self.rows_of(i) * r * out for i, (r, _, _) in enumerate(q.specs))
         return F
 
     def resident_bytes(self) -> int:
@@ -194,7 +243,7 @@ def oracle_step(wl: Workload):
     """fwd + bwd of the oracle on a sample of global rows of the workload (CPU legs only)."""
     from oracle import lora_oracle as O
     prepared = []
-    for q in wl.parts:
+    for q in getattr(wl, "cpu_parts", wl.parts):
         ads = [dict(A=O.bf16_to_f64(A), B=O.bf16_to_f64(B), alpha=a, p=p)
                for (A, B), (_, a, p) in zip(q.adapters, q.specs)]
         prepared.append((q, O.bf16_to_f64(q.W), ads))
@@ -321,16 +370,32 @@ def profiled_traffic(kernel: str, workload: str):
 # reference arm: the fp64 CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 
+def oracle_packer(lengths, adapters, capacity):
+    """The oracle's greedy packing, in the layout native.pack_microbatches returns (CPU legs only)."""
+    from oracle import lora_oracle as O
+    batch, row, nb = O.greedy_pack(lengths, capacity)
+    out = [{"segments": [], "samples": [], "valid": [], "rows": 0} for _ in range(nb)]
+    for i in sorted(range(len(lengths)), key=lambda i: (batch[i], row[i])):
+        b = out[batch[i]]
+        rows = O.padded_rows(lengths[i])
+        b["segments"].append((row[i], rows, int(adapters[i])))
+        b["samples"].append(i)
+        b["valid"].append(int(lengths[i]))
+        b["rows"] = row[i] + rows
+    return out
+
+
 def sample_rows(wl: Workload, rng, count: int):
-    count = int(np.clip(count, 1, wl.tokens))
-    return np.sort(rng.choice(wl.valid_rows, size=count, replace=False))
+    pool = wl.sample_pool
+    count = int(np.clip(count, 1, pool.size))
+    return np.sort(rng.choice(pool, size=count, replace=False))
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    wl = Workload(args.workload, args.m, args.r)
+    wl = Workload(args.workload, args.m, args.r, packer=oracle_packer)
     step = oracle_step(wl)
     rng = np.random.default_rng(0)
     probe = sample_rows(wl, rng, 32)
@@ -397,6 +462,13 @@ class DeviceProblem:
         m = wl.m
         self.inputs = {}   # name -> (pinned host, device); shared inputs appear once
         self.parts = []
+        shared = {}        # one device copy of a weight that several linears (microbatches) use
+
+        def weight(a):
+            if id(a) not in shared:
+                shared[id(a)] = pinned(a).to(dev)
+            return shared[id(a)]
+
         ws_need = (0, None)
         for q in wl.parts:
             if q.x_key not in self.inputs:
@@ -405,10 +477,10 @@ class DeviceProblem:
             dYh = pinned(q.dY)
             self.inputs["dY:" + q.label] = (dYh, dYh.to(dev))
             d = dict(part=q, X=self.inputs[q.x_key][1], dY=self.inputs["dY:" + q.label][1],
-                     W=pinned(q.W).to(dev), Y=torch.empty((m, q.n), dtype=bf, device=dev),
+                     W=weight(q.W), Y=torch.empty((m, q.n), dtype=bf, device=dev),
                      dX=torch.empty((m, q.k), dtype=bf, device=dev),
                      S=torch.empty((m, q.r_max), dtype=bf, device=dev),
-                     adapters=[api.Adapter(A=pinned(A).to(dev), B=pinned(B).to(dev), alpha=a, p=p,
+                     adapters=[api.Adapter(A=weight(A), B=weight(B), alpha=a, p=p,
                                            dA=torch.empty((q.k, r), dtype=bf, device=dev),
                                            dB=torch.empty((r, q.n), dtype=bf, device=dev))
                                for (A, B), (r, a, p) in zip(q.adapters, q.specs)])
@@ -586,7 +658,7 @@ def run_native(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = Workload(args.workload, args.m, args.r)
+    wl = Workload(args.workload, args.m, args.r, packer=native.pack_microbatches)
     stream = torch.cuda.current_stream(dev)
     prob = DeviceProblem(wl, dev, stream)
 
@@ -723,7 +795,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, LAYER])
+    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, GREEDY, LAYER])
     ap.add_argument("--m", type=int, default=None,
                     help="override the workload's token count (padded rows for the packed workload)")
     ap.add_argument("--r", type=int, default=None, help="override the rank of a single-adapter workload")

@@ -174,6 +174,26 @@ lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, in
 /* Host only: the keep threshold T for drop rate p (LORA_EINVAL outside [0,1)). */
 lora_status lora_keep_threshold(float p, uint32_t* T);
 
+/* Host only, no GPU needed: greedy token-capacity packing of samples into
+ * microbatches, the fallback packer of the LoRAFusion multi-adapter scheduler
+ * (notes on papers.chlience.com, section 5 "Multi-LoRA scheduler"; article,
+ * section 4.2 step 2).  First-fit decreasing: a sample occupies its length
+ * rounded up to whole 128-row tiles; samples are taken longest first (equal
+ * sizes in sample order) and each goes into the first microbatch, in opening
+ * order, with room left, else into a new one.
+ *   lengths[i]          tokens of sample i (>= 1), host array of n_samples
+ *   capacity            rows per microbatch, a positive multiple of 128
+ *   batch_of_sample[i]  receives the microbatch of sample i (0-based)
+ *   row_of_sample[i]    receives its first row there (samples of a microbatch
+ *                       lie back to back from row 0 in placement order)
+ *   *n_batches          receives the number of microbatches
+ * The samples of microbatch b with their rows and adapters form the segment
+ * table of a multi_lora_fwd / multi_lora_bwd call.  LORA_EINVAL for missing
+ * pointers, a length below 1 or a bad capacity; LORA_ESHAPE if a sample does
+ * not fit in one microbatch.  Nothing is written when the call fails. */
+lora_status lora_pack_greedy(const int64_t* lengths, int32_t n_samples, int64_t capacity,
+                             int32_t* batch_of_sample, int64_t* row_of_sample, int32_t* n_batches);
+
 /* Synchronises `stream`, then reads and clears the device status word of
  * `workspace`.  *code receives the raw device code (0 = none).  Returns
  * LORA_EDEVICE_TIMEOUT if a kernel gave up on a bounded wait. */

@@ -19,7 +19,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
 # Symbols include/lora.h declares, in declaration order.
 EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd",
             "lora_fwd_static_scratch", "lora_tile_table",
-            "lora_keep_threshold", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
+            "lora_keep_threshold", "lora_pack_greedy", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
             "lora_status_string", "lora_timing_begin", "lora_timing_end", "lora_kernel_name",
             "lora_last_error_string"]
 
@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             "lora_tile_table": (i32, [ctypes.POINTER(LoraSegment), i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                       i64]),
             "lora_keep_threshold": (i32, [f32, ctypes.POINTER(ctypes.c_uint32)]),
+            "lora_pack_greedy": (i32, [ctypes.POINTER(ctypes.c_int64), i32, i64, ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)]),
             "lora_device_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
             "lora_set_wait_limit_ns": (None, [u64]),
             "lora_debug_stuck_wait": (i32, [vp, sz, vp]),
@@ -122,6 +124,37 @@ def keep_threshold(p: float) -> int:
     T = ctypes.c_uint32(0)
     check("lora_keep_threshold", lib().lora_keep_threshold(ctypes.c_float(p), ctypes.byref(T)))
     return T.value
+
+
+def pack_greedy(lengths, capacity: int):
+    """Host-only greedy packing (first-fit decreasing) from the library.
+
+    Returns (batch_of_sample, row_of_sample, n_batches) as Python lists / int."""
+    n = len(lengths)
+    L = (ctypes.c_int64 * max(1, n))(*[int(x) for x in lengths])
+    B = (ctypes.c_int32 * max(1, n))()
+    R = (ctypes.c_int64 * max(1, n))()
+    nb = ctypes.c_int32(0)
+    check("lora_pack_greedy", lib().lora_pack_greedy(L, n, int(capacity), B, R, ctypes.byref(nb)))
+    return [B[i] for i in range(n)], [R[i] for i in range(n)], nb.value
+
+
+def pack_microbatches(lengths, adapters, capacity: int):
+    """Packs samples (token lengths and adapter ids) into microbatches of `capacity` rows.
+
+    Returns one dict per microbatch: "segments" [(row_start, rows, adapter)] in row order (the table
+    multi_lora_fwd / multi_lora_bwd take), "samples" (sample index per segment), "valid" (tokens per
+    segment) and "rows" (rows in use; the rest of the microbatch is free)."""
+    batch, row, nb = pack_greedy(lengths, capacity)
+    out = [{"segments": [], "samples": [], "valid": [], "rows": 0} for _ in range(nb)]
+    for i in sorted(range(len(lengths)), key=lambda i: (batch[i], row[i])):
+        b = out[batch[i]]
+        rows = -(-int(lengths[i]) // 128) * 128
+        b["segments"].append((row[i], rows, int(adapters[i])))
+        b["samples"].append(i)
+        b["valid"].append(int(lengths[i]))
+        b["rows"] = row[i] + rows
+    return out
 
 
 KERNEL_KINDS = 9

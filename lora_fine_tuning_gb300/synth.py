@@ -121,6 +121,20 @@ def packed_batch(seed: int, total_rows: int, n_adapters: int, *, mu: float = 6.2
     return batch
 
 
+def sample_stream(seed: int, target_rows: int, n_adapters: int, *, mu: float = 6.2, sigma: float = 0.6,
+                  lo: int = 64, hi: int = 2048):
+    """Samples of a global batch: lengths ~ lognormal(mu, sigma) clipped to [lo, hi] and uniform adapter
+    ids, drawn until their tile-padded rows reach target_rows.  Returns (lengths, adapters)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lengths, adapters, rows = [], [], 0
+    while rows < target_rows:
+        length = int(np.clip(np.round(rng.lognormal(mu, sigma)), lo, hi))
+        lengths.append(length)
+        adapters.append(int(rng.integers(0, n_adapters)))
+        rows += -(-length // TILE_ROWS) * TILE_ROWS
+    return lengths, adapters
+
+
 def multi_inputs(seed: int, k: int, n: int, specs: list, batch: PackedBatch, *, with_grad: bool = True):
     """Shared W, per-adapter (A_i, B_i), and X / dY with zero padding rows."""
     rng = np.random.Generator(np.random.PCG64(seed))

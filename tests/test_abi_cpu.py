@@ -121,3 +121,41 @@ def test_multi_validation_codes(lib):
     st = lib.multi_lora_bwd(256, 256, 256, ad, 2, native.segments_array([(0, 128, 0)]), 1, 0, 512, 64, 64, 256,
                             256, 256, 1 << 30, None)
     assert st == 1
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_pack_greedy_matches_oracle(lib, seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(0, 400))
+    lengths = np.clip(np.round(rng.lognormal(6.2, 0.6, size=n)), 1, 2048).astype(int).tolist()
+    capacity = int(128 * rng.choice([16, 32, 64, 128]))
+    got = native.pack_greedy(lengths, capacity)
+    if n == 0:
+        assert got == ([], [], 0)
+        return
+    assert got == O.greedy_pack(lengths, capacity)
+
+
+def test_pack_greedy_rejects(lib):
+    with pytest.raises(native.LoraError) as e:
+        native.pack_greedy([300], 256)
+    assert e.value.status == 3
+    for lengths, cap in (([10], 100), ([0], 256), ([10], 0)):
+        with pytest.raises(native.LoraError) as e:
+            native.pack_greedy(lengths, cap)
+        assert e.value.status == 1
+
+
+def test_pack_microbatches_make_valid_segment_tables(lib):
+    rng = np.random.default_rng(7)
+    lengths = np.clip(np.round(rng.lognormal(6.2, 0.6, size=300)), 64, 2048).astype(int).tolist()
+    adapters = rng.integers(0, 4, size=300).tolist()
+    batches = native.pack_microbatches(lengths, adapters, 16384)
+    seen = []
+    for b in batches:
+        # the segment table is accepted by the library's own router and by the oracle's
+        assert native.tile_table(b["segments"], 4, 16384) == O.tile_adapters(b["segments"], 16384, 4).tolist()
+        for (start, rows, a), i, v in zip(b["segments"], b["samples"], b["valid"]):
+            assert a == adapters[i] and v == lengths[i] and rows == O.padded_rows(v)
+        seen += b["samples"]
+    assert sorted(seen) == list(range(300))

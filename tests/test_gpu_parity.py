@@ -246,3 +246,18 @@ def test_workspace_is_left_zeroed():
     api.lora_bwd(dY, X, W, A, B, S, 1.0, 0.2, 51, ws=ws)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
+
+
+def test_greedy_packed_microbatches():
+    """A global batch packed by the library's greedy packer; every microbatch through the multi-adapter path."""
+    from lora_fine_tuning_gb300 import native
+    specs = MULTI_SPECS[:3]
+    k, n, cap, seed = 256, 384, 1024, 61
+    lengths, ads = synth.sample_stream(seed, 3 * cap, len(specs), mu=5.0, sigma=0.7, lo=16, hi=1000)
+    batches = native.pack_microbatches(lengths, ads, cap)
+    assert sum(len(b["samples"]) for b in batches) == len(lengths)
+    for b, mb in enumerate(batches):
+        pb = synth.PackedBatch(m=cap, segments=mb["segments"], valid=mb["valid"])
+        raw = synth.multi_inputs(seed + b, k, n, specs, pb)
+        adapters, Y, S, mask, dX = run_multi(k, n, mb["segments"], raw, specs, seed + b)
+        check_multi(k, n, mb["segments"], raw, specs, seed + b, adapters, Y, S, mask, dX)
