@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
 }
 
 // dA_a = bf16(acc_a) (k x r_a), accumulators cleared; dSq rows of active tiles cleared.
-__global__ void finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
+__global__ void __launch_bounds__(256, 4) finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
                                    int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap) {
     pdl_wait();
     pdl_trigger();
@@ -274,20 +274,22 @@ __global__ void finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint
     for (int a = 0; a < rt.n_adapters; ++a) {
         const AdapterDev ad = rt.ad[a];
         if (rt.adapter_begin[a + 1] == rt.adapter_begin[a]) continue;
-        const int g8 = ad.rank / 8;
-        const int64_t total = k * g8;
-        for (int64_t i = tid; i < total; i += stride) {
-            const int64_t j = i / g8;
+        // k * rank / 8 and m * ld / 8 stay below 2^31: 32-bit index arithmetic
+        const uint32_t g8 = static_cast<uint32_t>(ad.rank / 8);
+        const uint32_t total = static_cast<uint32_t>(k) * g8;
+        for (uint32_t i = static_cast<uint32_t>(tid); i < total; i += static_cast<uint32_t>(stride)) {
+            const uint32_t j = i / g8;
             const int c0 = static_cast<int>(i - j * g8) * 8;
-            finish_row(acc_base + ad.dA_off + j * ad.rpad + c0, dap.p[a] + j * ad.rank + c0, 8, 8, 1.0f);
+            finish_row(acc_base + ad.dA_off + static_cast<int64_t>(j) * ad.rpad + c0,
+                       dap.p[a] + static_cast<int64_t>(j) * ad.rank + c0, 8, 8, 1.0f);
         }
     }
-    const int g8 = ld / 8;
-    const int64_t total = m * g8;
-    for (int64_t i = tid; i < total; i += stride) {
-        const int64_t t = i / g8;
+    const uint32_t g8 = static_cast<uint32_t>(ld / 8);
+    const uint32_t total = static_cast<uint32_t>(m) * g8;
+    for (uint32_t i = static_cast<uint32_t>(tid); i < total; i += static_cast<uint32_t>(stride)) {
+        const uint32_t t = i / g8;
         if (rt.tile_adapter[t >> 7] < 0) continue;
-        stg128(dsq + t * ld + (i - t * g8) * 8, make_uint4(0u, 0u, 0u, 0u));
+        stg128(dsq + static_cast<int64_t>(t) * ld + (i - t * g8) * 8, make_uint4(0u, 0u, 0u, 0u));
     }
 }
 

@@ -256,19 +256,20 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
 
 // S'[t, c] = bf16(alpha_a / (1 - p_a) * S_acc[t, c]) for c < r_a, 0 for
 // r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.
-__global__ void finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
+__global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
                                   const __grid_constant__ Routing rt) {
     pdl_wait();
     pdl_trigger();
-    const int g8 = ld / 8;
-    const int64_t total = m * g8;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = i / g8;
+    // m * ld / 8 stays below 2^31: 32-bit index arithmetic
+    const uint32_t g8 = static_cast<uint32_t>(ld / 8);
+    const uint32_t total = static_cast<uint32_t>(m) * g8;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const uint32_t t = i / g8;
         const int c0 = static_cast<int>(i - t * g8) * 8;
         const int a = rt.tile_adapter[t >> 7];
         if (a < 0) continue;
-        finish_row(acc + t * ld + c0, out + t * ld + c0, rt.ad[a].rank - c0, 8, rt.ad[a].scale);
+        finish_row(acc + static_cast<int64_t>(t) * ld + c0, out + static_cast<int64_t>(t) * ld + c0,
+                   rt.ad[a].rank - c0, 8, rt.ad[a].scale);
     }
 }
 

@@ -245,27 +245,27 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
 // dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0, on
 // rows of active tiles; dB_a[c, j] = bf16(dB^T_acc_a[j, c]).  Every
 // accumulator read is cleared.
-__global__ void finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
+__global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
                                      float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
                                      const __grid_constant__ AdapterPtrs dbp) {
     pdl_wait();
     pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    // dS: one thread per 8 columns of a row
-    const int g8 = ld / 8;
-    const int64_t total_s = m * g8;
-    for (int64_t i = tid; i < total_s; i += stride) {
-        const int64_t t = i / g8;
+    // dS: one thread per 8 columns of a row (m * ld / 8 < 2^31: 32-bit index arithmetic)
+    const uint32_t g8 = static_cast<uint32_t>(ld / 8);
+    const uint32_t total_s = static_cast<uint32_t>(m) * g8;
+    for (uint32_t i = static_cast<uint32_t>(tid); i < total_s; i += static_cast<uint32_t>(stride)) {
+        const uint32_t t = i / g8;
         const int c0 = static_cast<int>(i - t * g8) * 8;
         const int a = rt.tile_adapter[t >> 7];
         if (a < 0) continue;
         const int valid = rt.ad[a].rank;
         float v[8];
         if (c0 < valid) {
-            float* src = dS_acc + t * ld + c0;
-            const float4 x = *reinterpret_cast<const float4*>(src);
-            const float4 y = *reinterpret_cast<const float4*>(src + 4);
+            float* src = dS_acc + static_cast<int64_t>(t) * ld + c0;
+            const float4 x = ld_l2_f4(src);
+            const float4 y = ld_l2_f4(src + 4);
             v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
             st_zero_f4(src);
             st_zero_f4(src + 4);
@@ -277,25 +277,46 @@ __global__ void finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __res
         pk.y = pack_bf16x2(v[2], v[3]);
         pk.z = pack_bf16x2(v[4], v[5]);
         pk.w = pack_bf16x2(v[6], v[7]);
-        stg128(dSq + t * ld + c0, pk);
+        stg128(dSq + static_cast<int64_t>(t) * ld + c0, pk);
     }
-    // dB: one thread per (4 ranks, column j); writes are coalesced along j
-    for (int a = 0; a < rt.n_adapters; ++a) {
+    // dB_a = (dB^T_acc_a)^T.  Lane i of a warp owns accumulator row j = 32 w + i (rpad floats, read 16 at a
+    // time, contiguous across the warp) and writes those values down column j of dB, so every store of the
+    // warp is 32 consecutive bf16 of one row of dB.  No shared memory, so under programmatic launch these
+    // CTAs can sit beside the CTAs of the GEMM that follows.
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = stride / 32, gw = tid / 32;
+    const int64_t per_adapter = (n + 31) / 32;   // warp tasks of one adapter; tasks of all adapters share the warps
+    int64_t tasks = 0;
+    for (int a = 0; a < rt.n_adapters; ++a)
+        if (rt.adapter_begin[a + 1] > rt.adapter_begin[a]) tasks += per_adapter;
+    for (int64_t w = gw; w < tasks; w += n_warps) {
+        int a = 0;
+        int64_t rem = w;
+        for (;; ++a) {
+            if (rt.adapter_begin[a + 1] == rt.adapter_begin[a]) continue;
+            if (rem < per_adapter) break;
+            rem -= per_adapter;
+        }
         const AdapterDev ad = rt.ad[a];
-        if (rt.adapter_begin[a + 1] == rt.adapter_begin[a]) continue;
-        const int64_t total = static_cast<int64_t>(ad.rank / 4) * n;
+        const int64_t j = rem * 32 + lane;
+        if (j >= n) continue;
         float* src = acc_base + ad.dB_off;
         uint16_t* dst = dbp.p[a];
-        for (int64_t i = tid; i < total; i += stride) {
-            const int64_t c4 = i / n;
-            const int64_t j = i - c4 * n;
-            float* q = src + j * ad.rpad + c4 * 4;
-            const float4 x = *reinterpret_cast<const float4*>(q);
-            st_zero_f4(q);
-            dst[(c4 * 4 + 0) * n + j] = bf16_bits(x.x);
-            dst[(c4 * 4 + 1) * n + j] = bf16_bits(x.y);
-            dst[(c4 * 4 + 2) * n + j] = bf16_bits(x.z);
-            dst[(c4 * 4 + 3) * n + j] = bf16_bits(x.w);
+        for (int c0 = 0; c0 < ad.rank; c0 += 16) {   // rpad is a power of two >= 16: whole float4 groups
+            float* q = src + j * ad.rpad + c0;
+            float v[16];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const float4 x = ld_l2_f4(q + 4 * g);
+                v[4 * g + 0] = x.x;
+                v[4 * g + 1] = x.y;
+                v[4 * g + 2] = x.z;
+                v[4 * g + 3] = x.w;
+                st_zero_f4(q + 4 * g);
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (c0 + e < ad.rank) dst[static_cast<int64_t>(c0 + e) * n + j] = bf16_bits(v[e]);
         }
     }
 }
