@@ -270,6 +270,35 @@ def dist_env():
     return ws, rank, local
 
 
+class Replicas:
+    """The ranks of a replicas-only run: one process per GPU, each running the whole layer on its own
+    tokens, with no collective on the data path.  The process group only lines the ranks up around a
+    timed region and takes the slowest rank's time (tensors live on `device`: the GPU under NCCL, the
+    CPU under gloo)."""
+
+    def __init__(self, world: int, device):
+        self.world, self.device = world, device
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step: int, steps: int, world: int, max_rank_ms: float) -> float:
+    """Whole-job tokens/s: the tokens every rank processed over the slowest rank's time (weak scaling)."""
+    return tokens_per_rank_step * steps * world / (max_rank_ms / 1e3)
+
+
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons while running."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
@@ -640,11 +669,11 @@ def e2e_leg(prob_a, prob_b, wl, dev, stream, steps, barrier, max_over_ranks, ws_
             raise RuntimeError("a kernel reported a bounded-wait timeout in the end-to-end leg")
     h2d = sum(h.numel() * h.element_size() for h, _ in sets[0].inputs.values())
     d2h = sum(h.numel() * h.element_size() for h in hosts[0])
-    return {"value": wl.tokens * steps * ws_n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": job_throughput(wl.tokens, steps, ws_n, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": ms / steps, "steps": steps,
             "overlap": "inputs of step i+1 and outputs of step i-1 copied on two copy streams while step i runs",
             "serial_ms_per_step": ms_serial / steps,
-            "serial_value": wl.tokens * steps * ws_n / (ms_serial / 1e3)}
+            "serial_value": job_throughput(wl.tokens, steps, ws_n, ms_serial)}
 
 
 def run_native(args):
@@ -672,16 +701,8 @@ def run_native(args):
         l2_note = (f"no flush: X/W/dY/Y/dX total {wl.resident_bytes() / 1e6:.0f} MB, larger than twice L2 "
                    f"({l2_bytes >> 20} MiB)")
 
-    def barrier():
-        if ws_n > 1:
-            dist.barrier()
-
-    def max_over_ranks(x: float) -> float:
-        if ws_n == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    replicas = Replicas(ws_n, dev)
+    barrier, max_over_ranks = replicas.barrier, replicas.max
 
     for _ in range(args.warmup):
         prob.step()
@@ -712,7 +733,7 @@ def run_native(args):
         raise RuntimeError("a kernel reported a bounded-wait timeout in the instrumented region")
 
     ms_per_step = elapsed_ms / args.steps
-    value = wl.tokens * args.steps * ws_n / (elapsed_ms / 1e3)
+    value = job_throughput(wl.tokens, args.steps, ws_n, elapsed_ms)
 
     # --- end to end through the public API with host buffers ---
     e2e = None
