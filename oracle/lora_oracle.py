@@ -375,3 +375,47 @@ def greedy_pack(lengths, capacity: int):
         row[i] = used[b]
         used[b] += sizes[i]
     return batch, row, len(used)
+
+
+# ---------------------------------------------------------------------------
+# DoRA: the LoRA layer with a learned magnitude per output feature
+# ---------------------------------------------------------------------------
+#
+# "Scaling DoRA" (paper.rainbus.top), background and method: the adapted
+# weight is split into a magnitude vector and a direction,
+#     W' = mag * (W + s B A) / ||W + s B A||   (norm over each output feature).
+# In this layer's orientation (Y = X W, W is k x n, the adapter adds
+# alpha * A B with A k x r, B r x n) the output features are the n columns, so
+#     g_j = mag_j / ||W[:, j] + alpha (A B)[:, j]||,
+#     Y   = g * (X W + alpha (dropout(X) A) B)      (g scales column j).
+# The pages say nothing about dropout here; the branch keeps the LoRA path's
+# dropout, so with p = 0 this is exactly X W'.  The pages do not fix the
+# backward either; the reading taken is that of DoRA's own training recipe:
+# the column norm is treated as a constant (no gradient flows through it), so
+#     dZ = dY * g,  (dX, dA, dB) = the LoRA backward of dZ,
+#     dmag_j = sum_t dY[t, j] Z[t, j] / ||W[:, j] + alpha (A B)[:, j]||,
+# with Z = X W + alpha S B the output before the column scale.
+
+
+def dora_column_norms(W, A, B, alpha: float) -> np.ndarray:
+    """||W[:, j] + alpha (A B)[:, j]||_2 for every output column j (the dense definition)."""
+    V = np.asarray(W, dtype=np.float64) + alpha * (np.asarray(A, dtype=np.float64) @ np.asarray(B, dtype=np.float64))
+    return np.sqrt((V * V).sum(axis=0))
+
+
+def dora_forward(X, W, A, B, mag, alpha: float, p: float, seed: int, rows=None):
+    """Returns (Y, S, D, g, Z): Y = g * Z with Z the LoRA output and g = mag / column norms."""
+    Z, S, D = lora_forward(X, W, A, B, alpha, p, seed, rows)
+    g = np.asarray(mag, dtype=np.float64) / dora_column_norms(W, A, B, alpha)
+    return Z * g, S, D, g, Z
+
+
+def dora_backward(dY, X, W, A, B, mag, alpha: float, p: float, seed: int, rows=None):
+    """Gradients with the column norm held constant.  Returns (dX, dA, dB, dmag)."""
+    norms = dora_column_norms(W, A, B, alpha)
+    g = np.asarray(mag, dtype=np.float64) / norms
+    Z, _, _ = lora_forward(X, W, A, B, alpha, p, seed, rows)
+    dY = np.asarray(dY, dtype=np.float64)
+    dX, dA, dB, _ = lora_backward(dY * g, X, W, A, B, alpha, p, seed, rows)
+    dmag = (dY * Z).sum(axis=0) / norms
+    return dX, dA, dB, dmag
