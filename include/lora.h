@@ -137,6 +137,46 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
                            int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX,
                            void* workspace, size_t workspace_bytes, void* stream);
 
+/* DoRA ("Scaling DoRA", paper.rainbus.top): the adapted weight split into a
+ * magnitude per output feature and a direction,
+ *     W' = mag * (W + alpha A B) / ||W + alpha A B||  (norm over each column j),
+ *     Y  = g * (X W + alpha (dropout(X) A) B),  g_j = mag_j / ||W_j + alpha (A B)_j||,
+ * in this layer's orientation (W k x n, so the n output features are columns).
+ * The norm comes from the pages' factored identity
+ *     ||W_j||^2 + 2 alpha B_j . (W^T A)_j + alpha^2 B_j^T (A^T A) B_j,
+ * never from the dense k x n update.  Single adapter; rank, p, alignment and
+ * shape rules as for lora_fwd.  mag, w_norm2, g_saved and dmag are fp32
+ * vectors of n, 16-byte aligned. */
+
+/* Workspace bytes for dora_fwd / dora_bwd: lora_workspace_size(m, k, n, r, 1)
+ * plus the DoRA accumulators (W^T A, A^T A, dmag).  Same contract as the LoRA
+ * workspace: zero before the first call, and every completed call leaves it
+ * zero. */
+size_t dora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r);
+
+/* w_norm2[j] = ||W[:, j]||^2 in fp32 (W k x n is frozen: compute once and
+ * pass to every dora_fwd).  Asynchronous on `stream`. */
+lora_status dora_weight_norm2(const lora_bf16* W, int64_t k, int64_t n, float* w_norm2, void* stream);
+
+/* DoRA forward: writes Y (m x n), S_saved (as lora_fwd), g_saved (n: the
+ * column scale, needed by dora_bwd) and optionally mask_bits. */
+lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B, const float* mag,
+                     const float* w_norm2, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
+                     int32_t r, lora_bf16* Y, lora_bf16* S_saved, float* g_saved, uint8_t* mask_bits, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* DoRA backward with the column norm held constant (as DoRA trains; the pages
+ * fix no backward): dZ = dY * g feeds the LoRA backward, giving dX, dA, dB;
+ * dmag_j = sum_t dY[t, j] Y[t, j] / mag_j (= sum_t dY Z / ||.||_j).  Inputs
+ * are the forward's X, W, A, B, S_saved, Y, mag, g_saved and the same alpha,
+ * p, seed.  dZ: caller scratch of m x n bf16 (16-byte aligned; its contents
+ * before and after the call do not matter). */
+lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
+                     const lora_bf16* B, const lora_bf16* S_saved, const lora_bf16* Y, const float* mag,
+                     const float* g_saved, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
+                     int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, float* dmag, lora_bf16* dZ,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
 /* lora_fwd for callers that cannot allocate device memory (no counterpart in
  * the LoRAFusion write-ups; it only changes where the scratch lives).
  * Some callers have no way to hand the library a workspace: a plugin whose
@@ -218,7 +258,7 @@ const char* lora_status_string(lora_status s);
  * 1 finalize S, 2 forward GEMM, 3 dS/dB, 4 finalize dS/dB, 5 backward GEMM,
  * 6 dA, 7 finalize dA, 8 memset (gradients of adapters that own no rows).
  * Host-side cost: two event records per launch. */
-enum { LORA_KERNEL_KINDS = 9 };
+enum { LORA_KERNEL_KINDS = 13 };
 lora_status lora_timing_begin(void);
 lora_status lora_timing_end(float* total_ms, int32_t* launches, int32_t n_kinds);
 const char* lora_kernel_name(int32_t kind);

@@ -172,6 +172,84 @@ def multi_lora_bwd(dY, X, W, adapters: Sequence[Adapter], segments, seed: int, S
     return dX
 
 
+_DORA_WS: dict = {}
+
+
+def dora_workspace(m: int, k: int, n: int, r: int, device=None) -> torch.Tensor:
+    """A cached, zero-initialised workspace for dora_fwd / dora_bwd with these sizes."""
+    device = torch.device(device or torch.cuda.current_device())
+    size = int(native.lib().dora_workspace_size(m, k, n, r))
+    ws = _DORA_WS.get(device.index)
+    if ws is None or ws.numel() < size:
+        ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=device)
+        _DORA_WS[device.index] = ws
+    return ws
+
+
+def _check_f32(name: str, t: torch.Tensor, n: int) -> None:
+    if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != n:
+        raise ValueError(f"{name} must be a contiguous CUDA float32 vector of {n}")
+
+
+def dora_weight_norm2(W, stream=None):
+    """Column norms squared of the frozen weight, fp32 (computed once per weight)."""
+    k, n = W.shape
+    _check_bf16("W", W, (k, n))
+    out = torch.empty(n, dtype=torch.float32, device=W.device)
+    native.check("dora_weight_norm2", native.lib().dora_weight_norm2(_ptr(W), k, n, _ptr(out), _stream(stream)))
+    return out
+
+
+def dora_fwd(X, W, A, B, mag, w_norm2, alpha: float, p: float, seed: int, *, Y=None, S_saved=None, g_saved=None,
+             mask_bits=None, want_mask: bool = False, ws=None, stream=None):
+    """DoRA forward: Y = g * (X W + alpha (dropout(X) A) B) with g = mag / column norms of W + alpha A B.
+    Returns (Y, S_saved, g_saved, mask_bits or None)."""
+    m, k = X.shape
+    n = W.shape[1]
+    r = A.shape[1]
+    for name, t, shp in (("X", X, (m, k)), ("W", W, (k, n)), ("A", A, (k, r)), ("B", B, (r, n))):
+        _check_bf16(name, t, shp)
+    _check_f32("mag", mag, n)
+    _check_f32("w_norm2", w_norm2, n)
+    Y = Y if Y is not None else torch.empty((m, n), dtype=torch.bfloat16, device=X.device)
+    S_saved = S_saved if S_saved is not None else torch.empty((m, r), dtype=torch.bfloat16, device=X.device)
+    g_saved = g_saved if g_saved is not None else torch.empty(n, dtype=torch.float32, device=X.device)
+    if want_mask and mask_bits is None:
+        mask_bits = torch.empty((m, k // 8), dtype=torch.uint8, device=X.device)
+    ws = ws if ws is not None else dora_workspace(m, k, n, r)
+    st = native.lib().dora_fwd(_ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(mag), _ptr(w_norm2), float(alpha), float(p),
+                               int(seed) & (2**64 - 1), m, k, n, r, _ptr(Y), _ptr(S_saved), _ptr(g_saved),
+                               _ptr(mask_bits), _ptr(ws), ws.numel(), _stream(stream))
+    native.check("dora_fwd", st)
+    return Y, S_saved, g_saved, mask_bits
+
+
+def dora_bwd(dY, X, W, A, B, S_saved, Y, mag, g_saved, alpha: float, p: float, seed: int, *, dX=None, dA=None,
+             dB=None, dmag=None, dZ=None, ws=None, stream=None):
+    """DoRA backward with the column norm held constant.  Returns (dX, dA, dB, dmag).
+    dZ: m x n bf16 scratch (allocated if not given)."""
+    m, k = X.shape
+    n = W.shape[1]
+    r = A.shape[1]
+    for name, t, shp in (("dY", dY, (m, n)), ("X", X, (m, k)), ("W", W, (k, n)), ("A", A, (k, r)),
+                         ("B", B, (r, n)), ("S_saved", S_saved, (m, r)), ("Y", Y, (m, n))):
+        _check_bf16(name, t, shp)
+    _check_f32("mag", mag, n)
+    _check_f32("g_saved", g_saved, n)
+    dX = dX if dX is not None else torch.empty((m, k), dtype=torch.bfloat16, device=X.device)
+    dA = dA if dA is not None else torch.empty((k, r), dtype=torch.bfloat16, device=X.device)
+    dB = dB if dB is not None else torch.empty((r, n), dtype=torch.bfloat16, device=X.device)
+    dmag = dmag if dmag is not None else torch.empty(n, dtype=torch.float32, device=X.device)
+    dZ = dZ if dZ is not None else torch.empty((m, n), dtype=torch.bfloat16, device=X.device)
+    _check_bf16("dZ", dZ, (m, n))
+    ws = ws if ws is not None else dora_workspace(m, k, n, r)
+    st = native.lib().dora_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(S_saved), _ptr(Y), _ptr(mag),
+                               _ptr(g_saved), float(alpha), float(p), int(seed) & (2**64 - 1), m, k, n, r, _ptr(dX),
+                               _ptr(dA), _ptr(dB), _ptr(dmag), _ptr(dZ), _ptr(ws), ws.numel(), _stream(stream))
+    native.check("dora_bwd", st)
+    return dX, dA, dB, dmag
+
+
 def lora_device_status(ws: torch.Tensor, stream=None) -> int:
     """Synchronises the stream; returns the raw device status code of the workspace (0 = fine) and clears it."""
     code = ctypes.c_int32(0)

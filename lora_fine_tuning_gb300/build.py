@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblora_gb300.so")
 
-SOURCES = ["api.cu", "k_down.cu", "k_gemm2.cu", "k_dsdb.cu", "k_da.cu", "pack.cu"]
+SOURCES = ["api.cu", "k_down.cu", "k_gemm2.cu", "k_dsdb.cu", "k_da.cu", "k_dora.cu", "pack.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

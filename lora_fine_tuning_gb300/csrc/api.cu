@@ -42,9 +42,13 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 // optional per-kernel timing (measurement tools): events around each launch
 // ---------------------------------------------------------------------------
 
-enum Kind : int { kDownProj = 0, kFinalizeS, kGemmFwd, kDsDb, kFinalize, kGemmBwd, kDa, kFinalizeDa, kMemset, kKinds };
+enum Kind : int {
+    kDownProj = 0, kFinalizeS, kGemmFwd, kDsDb, kFinalize, kGemmBwd, kDa, kFinalizeDa, kMemset,
+    kDoraU, kDoraNorm, kDoraDz, kDoraDmag, kKinds
+};
 const char* const kKindNames[kKinds] = {"down_proj", "finalize_s", "gemm_fwd", "ds_db", "finalize_ds_db",
-                                        "gemm_bwd", "da", "finalize_da", "memset"};
+                                        "gemm_bwd", "da", "finalize_da", "memset",
+                                        "dora_u", "dora_norm", "dora_dz", "dora_dmag"};
 
 struct TimingRec {
     int kind;
@@ -96,7 +100,7 @@ lora_status device_setup(int* sms_out) {
             d.sms = sms;
             if (!cuda_ok(down_configure()) || !cuda_ok(gemm2_configure()) ||
                 !cuda_ok(dsdb_configure()) ||
-                !cuda_ok(da_configure()))
+                !cuda_ok(da_configure()) || !cuda_ok(dora_configure()))
                 d.status = LORA_ECUDA;
         }
         if (d.status == LORA_OK && g_encode == nullptr) {
@@ -310,8 +314,21 @@ DevCtl ctl_of(const Call& c) { return DevCtl{reinterpret_cast<int*>(c.ws + c.L.s
         if (!cuda_ok(expr)) return LORA_ECUDA;   \
     } while (0)
 
+// DoRA's extra inputs and scratch for one forward (single adapter).
+struct DoraFwd {
+    const float* mag;     // n
+    const float* wn2;     // n: ||W[:, j]||^2
+    float* g_out;         // n: the column scale (saved for the backward)
+    float* U;             // workspace: n x rpad fp32 (zero between calls)
+    float* G;             // workspace: r x r fp32
+};
+
+lora_status run_dora_norm(const Call& c, const DoraFwd& d, const uint16_t* W, const lora_adapter& ad, int64_t k,
+                          int64_t n);
+
 lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const lora_adapter* ads, uint64_t seed,
-                    int64_t m, int64_t k, int64_t n, uint16_t* Y, uint16_t* S_saved, uint8_t* mask_bits) {
+                    int64_t m, int64_t k, int64_t n, uint16_t* Y, uint16_t* S_saved, uint8_t* mask_bits,
+                    const DoraFwd* dora = nullptr) {
     if (m == 0) return LORA_OK;
     const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
     const int nad = c.rt.n_adapters;
@@ -365,6 +382,11 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     g.nkb = static_cast<int32_t>((k + 63) / 64);
     g.seed_lo = seed_lo;
     g.seed_hi = seed_hi;
+    if (dora) {
+        const lora_status st = run_dora_norm(c, *dora, W, ads[0], k, n);
+        if (st) return st;
+        g.col_scale = dora->g_out;
+    }
     LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm2(g, false, 256, c.sms, c.stream); }));
     return LORA_OK;
 }
@@ -480,6 +502,76 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(p, c.sms, c.stream); }));
     }
     return LORA_OK;
+}
+
+// DoRA column scale g_j = mag_j / ||W_j + alpha (A B)_j|| from the factored norm: U = W^T A by the dA
+// kernel (W's k rows stand in for the tokens, A for dSq, no mask), G = A^T A, then one thread per column.
+lora_status run_dora_norm(const Call& c, const DoraFwd& d, const uint16_t* W, const lora_adapter& ad, int64_t k,
+                          int64_t n) {
+    const int r = ad.rank, rp = rank_pad(r);
+    const int64_t n_tiles = (k + kTileM - 1) / kTileM;
+    if (n_tiles > kMaxTiles) return LORA_ESHAPE;
+    static DaParams pu;
+    std::memset(&pu, 0, sizeof(pu));
+    if (!make_map(&pu.mapX, W, n, k, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+    if (!make_map(&pu.mapD[0], ad.A, r, k, r, std::min(rp, 64), 128, rank_swizzle_host(rp))) return LORA_ECUDA;
+    Routing& rt = pu.rt;
+    rt.n_tiles = static_cast<int32_t>(n_tiles);
+    rt.n_active = static_cast<int32_t>(n_tiles);
+    rt.n_adapters = 1;
+    rt.rpad_max = rp;
+    rt.adapter_begin[0] = 0;
+    for (int a = 1; a <= kMaxAdapters; ++a) rt.adapter_begin[a] = static_cast<int32_t>(n_tiles);
+    rt.ad[0].rank = r;
+    rt.ad[0].rpad = rp;
+    rt.ad[0].T = 0;          // no dropout: the plain contraction W^T A
+    rt.ad[0].scale = 1.f;
+    rt.ad[0].dA_off = 0;
+    for (int64_t t = 0; t < n_tiles; ++t) {
+        rt.tile_adapter[t] = 0;
+        rt.active_tiles[t] = static_cast<uint16_t>(t);
+    }
+    pu.ctl = ctl_of(c);
+    pu.acc_base = d.U;
+    pu.ld = r;
+    pu.m = k;
+    pu.k = n;
+    pu.nfb = static_cast<int32_t>((n + 127) / 128);
+    pu.units = static_cast<int64_t>(pu.nfb) * n_tiles;
+    pu.unit_begin[0] = 0;
+    for (int a = 1; a <= kMaxAdapters; ++a) pu.unit_begin[a] = pu.units;
+    pu.off_d = 32768;
+    pu.stage_bytes = pu.off_d + 256 * static_cast<uint32_t>(rp);
+    pu.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / pu.stage_bytes));
+    const int grid = static_cast<int>(std::min<int64_t>(pu.units, c.sms));
+    LORA_CUDA(timed(kDoraU, c.stream, [&] { return launch_da(pu, grid, c.stream); }));
+    LORA_CUDA(timed(kDoraNorm, c.stream, [&] {
+        cudaError_t e = launch_dora_gram(ad.A, k, r, d.G, c.stream);
+        if (e != cudaSuccess) return e;
+        return launch_dora_scale(d.U, rp, ad.B, d.G, r, d.wn2, d.mag, ad.alpha, n, d.g_out, c.stream);
+    }));
+    // G's last reader is done: back to zero, like every other accumulator of the workspace
+    LORA_CUDA(cudaMemsetAsync(d.G, 0, static_cast<size_t>(r) * r * 4, c.stream));
+    return LORA_OK;
+}
+
+// DoRA accumulators after the LoRA workspace: U (n x rpad fp32), G (r x r fp32), dmag (n fp32).  Like the
+// rest of the workspace they are zero between calls: their last readers clear them.
+struct DoraLayout {
+    size_t u = 0, g = 0, dmag = 0, total = 0;
+};
+
+DoraLayout dora_layout(size_t base, int64_t n, int r) {
+    DoraLayout D;
+    size_t off = up(base);
+    D.u = off;
+    off = up(off + static_cast<size_t>(n) * rank_pad(r) * 4);
+    D.g = off;
+    off = up(off + static_cast<size_t>(r) * r * 4);
+    D.dmag = off;
+    off = up(off + static_cast<size_t>(n) * 4);
+    D.total = off;
+    return D;
 }
 
 std::mutex g_call_mu;  // the static parameter blocks above are shared
@@ -683,6 +775,80 @@ const char* lora_status_string(lora_status s) {
         case LORA_ETABLE: return "invalid segment table";
     }
     return "unknown status";
+}
+
+size_t dora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r) {
+    if (m < 0 || k < 0 || n < 0 || r < 0) return 0;
+    return dora_layout(lora_workspace_size(m, k, n, r, 1), n, std::max(r, 8)).total;
+}
+
+lora_status dora_weight_norm2(const lora_bf16* W, int64_t k, int64_t n, float* w_norm2, void* stream) {
+    if (!W || !w_norm2) return LORA_EINVAL;
+    if (k <= 0 || n <= 0 || n % 8) return LORA_ESHAPE;
+    if (!aligned16(W) || !aligned16(w_norm2)) return LORA_EALIGN;
+    int sms = 0;
+    lora_status st;
+    {
+        std::lock_guard<std::mutex> lock(g_call_mu);
+        st = device_setup(&sms);
+    }
+    if (st) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!cuda_ok(cudaMemsetAsync(w_norm2, 0, static_cast<size_t>(n) * 4, s))) return LORA_ECUDA;
+    if (!cuda_ok(launch_dora_norm2(W, k, n, w_norm2, sms, s))) return LORA_ECUDA;
+    return LORA_OK;
+}
+
+lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B, const float* mag,
+                     const float* w_norm2, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
+                     int32_t r, lora_bf16* Y, lora_bf16* S_saved, float* g_saved, uint8_t* mask_bits, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    if (!W || !mag || !w_norm2 || !g_saved || (m > 0 && (!X || !Y || !S_saved))) return LORA_EINVAL;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved) || !aligned16(mag) ||
+        !aligned16(w_norm2) || !aligned16(g_saved))
+        return LORA_EALIGN;
+    lora_adapter ad{r, alpha, p, A, B, nullptr, nullptr};
+    lora_segment seg{0, m, 0, 0};
+    std::lock_guard<std::mutex> lock(g_call_mu);
+    static Call c;
+    lora_status st = prepare(c, &ad, 1, &seg, m > 0 ? 1 : 0, m, k, n, false, workspace, workspace_bytes, stream);
+    if (st) return st;
+    const DoraLayout D = dora_layout(c.L.total, n, r);
+    if (workspace_bytes < D.total) return LORA_EWORKSPACE;
+    DoraFwd d{mag, w_norm2, g_saved, reinterpret_cast<float*>(c.ws + D.u), reinterpret_cast<float*>(c.ws + D.g)};
+    if (m == 0) {
+        // no tokens: the column scale is still defined (the backward reads it)
+        return run_dora_norm(c, d, W, ad, k, n);
+    }
+    return run_fwd(c, X, W, &ad, seed, m, k, n, Y, S_saved, mask_bits, &d);
+}
+
+lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
+                     const lora_bf16* B, const lora_bf16* S_saved, const lora_bf16* Y, const float* mag,
+                     const float* g_saved, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
+                     int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, float* dmag, lora_bf16* dZ,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (!W || !mag || !g_saved || !dmag || (m > 0 && (!X || !dY || !dX || !Y || !S_saved || !dZ)))
+        return LORA_EINVAL;
+    if (!aligned16(dY) || !aligned16(X) || !aligned16(W) || !aligned16(dX) || !aligned16(S_saved) ||
+        !aligned16(Y) || !aligned16(mag) || !aligned16(g_saved) || !aligned16(dmag) || !aligned16(dZ))
+        return LORA_EALIGN;
+    lora_adapter ad{r, alpha, p, A, B, dA, dB};
+    lora_segment seg{0, m, 0, 0};
+    std::lock_guard<std::mutex> lock(g_call_mu);
+    static Call c;
+    lora_status st = prepare(c, &ad, 1, &seg, m > 0 ? 1 : 0, m, k, n, true, workspace, workspace_bytes, stream);
+    if (st) return st;
+    const DoraLayout D = dora_layout(c.L.total, n, r);
+    if (workspace_bytes < D.total) return LORA_EWORKSPACE;
+    float* dmag_acc = reinterpret_cast<float*>(c.ws + D.dmag);
+    if (m > 0)
+        LORA_CUDA(timed(kDoraDz, c.stream, [&] { return launch_dora_dz(dY, Y, g_saved, m, n, dZ, dmag_acc, c.sms,
+                                                                      c.stream); }));
+    st = run_bwd(c, dZ, X, W, &ad, seed, m, k, n, S_saved, dX);
+    if (st) return st;
+    LORA_CUDA(timed(kDoraDmag, c.stream, [&] { return launch_dora_dmag(dmag_acc, mag, n, dmag, c.stream); }));
+    return LORA_OK;
 }
 
 }  // extern "C"

@@ -331,6 +331,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 } else {
                     tmem_ld_wait();
                 }
+                if (!kBwd && p.col_scale != nullptr) {
+                    // DoRA: column j of the output times g_j (columns past N read nothing; the store clips them)
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int64_t col = static_cast<int64_t>(n0) + c * 16 + e;
+                        const float gsc = col < p.N ? __ldg(p.col_scale + col) : 0.f;
+                        v[e] = __float_as_uint(__uint_as_float(v[e]) * gsc);
+                    }
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     packed[c * 8 + e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));

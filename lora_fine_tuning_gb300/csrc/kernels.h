@@ -57,4 +57,14 @@ cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream);
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream);
 
+// DoRA pieces (k_dora.cu); the dA kernel also computes DoRA's U = W^T A.
+cudaError_t dora_configure();
+cudaError_t launch_dora_norm2(const uint16_t* W, int64_t k, int64_t n, float* out, int sms, cudaStream_t stream);
+cudaError_t launch_dora_gram(const uint16_t* A, int64_t k, int r, float* G, cudaStream_t stream);
+cudaError_t launch_dora_scale(float* U, int rpad, const uint16_t* B, const float* G, int r, const float* wn2,
+                              const float* mag, float alpha, int64_t n, float* g_out, cudaStream_t stream);
+cudaError_t launch_dora_dz(const uint16_t* dY, const uint16_t* Y, const float* g, int64_t m, int64_t n, uint16_t* dZ,
+                           float* dmag_acc, int sms, cudaStream_t stream);
+cudaError_t launch_dora_dmag(float* dmag_acc, const float* mag, int64_t n, float* dmag, cudaStream_t stream);
+
 }  // namespace lora

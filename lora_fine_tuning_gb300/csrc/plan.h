@@ -84,6 +84,7 @@ struct GemmParams {
     int64_t M, N, K;                   // GEMM sizes: fwd (m, n, k), bwd (m, k, n)
     int32_t nkb;                       // 64-deep K blocks of the main product
     uint32_t seed_lo, seed_hi;
+    const float* col_scale;            // forward only, optional: output column j is multiplied by col_scale[j] (DoRA)
 };
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,

@@ -18,6 +18,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
 
 # Symbols include/lora.h declares, in declaration order.
 EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd",
+            "dora_workspace_size", "dora_weight_norm2", "dora_fwd", "dora_bwd",
             "lora_fwd_static_scratch", "lora_tile_table",
             "lora_keep_threshold", "lora_pack_greedy", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
             "lora_status_string", "lora_timing_begin", "lora_timing_end", "lora_kernel_name",
@@ -67,6 +68,12 @@ def lib() -> ctypes.CDLL:
                                      i64, i64, i64, vp, vp, vp, vp, sz, vp]),
             "multi_lora_bwd": (i32, [vp, vp, vp, ctypes.POINTER(LoraAdapter), i32, ctypes.POINTER(LoraSegment), i32,
                                      u64, i64, i64, i64, vp, vp, vp, sz, vp]),
+            "dora_workspace_size": (sz, [i64, i64, i64, i32]),
+            "dora_weight_norm2": (i32, [vp, i64, i64, vp, vp]),
+            "dora_fwd": (i32, [vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, vp, sz,
+                               vp]),
+            "dora_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp,
+                               vp, vp, vp, sz, vp]),
             "lora_fwd_static_scratch": (i32, [vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp]),
             "lora_tile_table": (i32, [ctypes.POINTER(LoraSegment), i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                       i64]),
@@ -157,7 +164,7 @@ def pack_microbatches(lengths, adapters, capacity: int):
     return out
 
 
-KERNEL_KINDS = 9
+KERNEL_KINDS = 13
 
 
 def timing_begin() -> None:

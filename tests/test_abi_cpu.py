@@ -159,3 +159,17 @@ def test_pack_microbatches_make_valid_segment_tables(lib):
             assert a == adapters[i] and v == lengths[i] and rows == O.padded_rows(v)
         seen += b["samples"]
     assert sorted(seen) == list(range(300))
+
+
+def test_dora_workspace_and_validation(lib):
+    assert lib.dora_workspace_size(1024, 512, 512, 16) > lib.lora_workspace_size(1024, 512, 512, 16, 1)
+    # null magnitude vector / misaligned pointers are rejected before any CUDA call
+    st = lib.dora_fwd(256, 256, 256, 256, None, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256, None, 256,
+                      1 << 30, None)
+    assert st == 1
+    st = lib.dora_fwd(256, 256, 256, 256, 260, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256, None, 256,
+                      1 << 30, None)
+    assert st == 2
+    st = lib.dora_bwd(256, 256, 256, 256, 256, 256, 256, 256, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256,
+                      None, 256, 256, 1 << 30, None)
+    assert st == 1
