@@ -53,14 +53,16 @@ def load_peaks():
 MULTI = "multi_4ad"      # packed batch, four adapters with ranks 16/16/32/64 on one 8192x8192 weight
 GREEDY = "multi_4ad_greedy"   # a global batch of the same samples packed into 16384-row microbatches (greedy)
 LAYER = "llama8b_layer"  # the seven LoRA projections of one Llama-3.1-8B decoder layer
+DORA = "dora8b_up"       # the Llama-3.1-8B up-proj layer as DoRA (magnitude per output column)
 
 
 class Part:
     """One LoRA linear of a workload: its shapes, weight, adapters, inputs and (packed) segments."""
 
-    def __init__(self, label, k, n, specs, seed, X, W, dY, adapters, segments=None, x_key="X"):
+    def __init__(self, label, k, n, specs, seed, X, W, dY, adapters, segments=None, x_key="X", mag=None):
         self.label, self.k, self.n, self.specs, self.seed = label, k, n, specs, seed
         self.X, self.W, self.dY, self.adapters, self.segments, self.x_key = X, W, dY, adapters, segments, x_key
+        self.mag = mag          # DoRA: magnitude per output column (fp32), else None
 
     @property
     def single(self) -> bool:
@@ -138,15 +140,21 @@ class Workload:
             self.owner = np.zeros(self.m, dtype=np.int64)
             self.valid_rows = np.arange(self.m)
         else:
-            cfg = dict(synth.WORKLOADS[name])
+            cfg = dict(synth.WORKLOADS["llama8b_up" if name == DORA else name])
             if m:
                 cfg["m"] = m
             if r:
                 cfg["r"] = r
             self.m = cfg["m"]
             raw = synth.layer_inputs(cfg["seed"], self.m, cfg["k"], cfg["n"], cfg["r"])
+            mag = None
+            if name == DORA:
+                # magnitudes near their initial values (the column norms of W), seeded
+                Wf = (raw["W"].astype(np.uint32) << 16).view(np.float32)
+                rng = np.random.Generator(np.random.PCG64(cfg["seed"] + 100))
+                mag = (np.sqrt((Wf.astype(np.float64) ** 2).sum(0)) * rng.uniform(0.8, 1.2, cfg["n"])).astype(np.float32)
             self.parts = [Part(name, cfg["k"], cfg["n"], [(cfg["r"], cfg["alpha"], cfg["p"])], cfg["seed"],
-                               raw["X"], raw["W"], raw["dY"], [(raw["A"], raw["B"])])]
+                               raw["X"], raw["W"], raw["dY"], [(raw["A"], raw["B"])], mag=mag)]
             self.owner = np.zeros(self.m, dtype=np.int64)
             self.valid_rows = np.arange(self.m)
 
@@ -190,7 +198,8 @@ class Workload:
                     f"tokens, r={r}, alpha={alpha}, p={p}; attention, norms and activations not included")
         q = self.parts[0]
         r, alpha, p = q.specs[0]
-        return f"{self.name}: LoRA linear m={self.m} tokens, k={q.k}, n={q.n}, r={r}, alpha={alpha}, p={p}, seed={q.seed}"
+        kind = "DoRA linear (column magnitudes, norm held constant in the backward)" if q.mag is not None else "LoRA linear"
+        return f"{self.name}: {kind} m={self.m} tokens, k={q.k}, n={q.n}, r={r}, alpha={alpha}, p={p}, seed={q.seed}"
 
     def layer_flops(self) -> int:
         """Algorithmic FLOPs of one fwd+bwd over the valid tokens: per linear 4Tkn + sum_i 6 T_i r_i (k+n)
@@ -199,6 +208,9 @@ class Workload:
         for q in (self.parts[:1] if self.name == GREEDY else self.parts):
             F += 4 * self.tokens * q.k * q.n
             F += sum(6 * self.tokens_of(i) * r * (q.k + q.n) for i, (r, _, _) in enumerate(q.specs))
+            if q.mag is not None:   # DoRA's column norm: U = W^T A (2knr) and G = A^T A (2kr^2)
+                r = q.specs[0][0]
+                F += 2 * q.k * q.n * r + 2 * q.k * r * r
         return F
 
     def layer_bytes(self) -> int:
@@ -217,6 +229,9 @@ class Workload:
                 Ti = self.tokens_of(i)
                 fwd += k * r + r * n + Ti * r
                 bwd += Ti * r + 2 * (k * r + r * n)
+            if q.mag is not None:   # DoRA: W again for U; bwd reads Y and writes + reads dZ = dY * g
+                fwd += k * n
+                bwd += 3 * T * n
             total += fwd + bwd
         return 2 * total
 
@@ -252,7 +267,11 @@ def oracle_step(wl: Workload):
         for q, W, ads in prepared:
             X = O.bf16_to_f64(q.X[rows])
             dY = O.bf16_to_f64(q.dY[rows])
-            if q.single:
+            if q.mag is not None:
+                ad = ads[0]
+                O.dora_forward(X, W, ad["A"], ad["B"], q.mag, ad["alpha"], ad["p"], q.seed, rows=rows)
+                O.dora_backward(dY, X, W, ad["A"], ad["B"], q.mag, ad["alpha"], ad["p"], q.seed, rows=rows)
+            elif q.single:
                 ad = ads[0]
                 O.lora_forward(X, W, ad["A"], ad["B"], ad["alpha"], ad["p"], q.seed, rows=rows)
                 O.lora_backward(dY, X, W, ad["A"], ad["B"], ad["alpha"], ad["p"], q.seed, rows=rows)
@@ -513,15 +532,29 @@ class DeviceProblem:
                                            dA=torch.empty((q.k, r), dtype=bf, device=dev),
                                            dB=torch.empty((r, q.n), dtype=bf, device=dev))
                                for (A, B), (r, a, p) in zip(q.adapters, q.specs)])
+            if q.mag is not None:
+                d["mag"] = torch.from_numpy(q.mag).to(dev)
+                d["wn2"] = api.dora_weight_norm2(d["W"])          # W is frozen: once, outside any timed region
+                d["g"] = torch.empty(q.n, dtype=torch.float32, device=dev)
+                d["dmag"] = torch.empty(q.n, dtype=torch.float32, device=dev)
+                d["dZ"] = torch.empty((m, q.n), dtype=bf, device=dev)
             self.parts.append(d)
             size = api.lora_workspace_size(m, q.k, q.n, max(8, q.r_max), len(q.adapters))
             if size > ws_need[0]:
                 ws_need = (size, (m, q.k, q.n, max(8, q.r_max), len(q.adapters)))
-        self.ws = api.workspace(*ws_need[1], device=dev)
+        if any(q.mag is not None for q in wl.parts):
+            q = wl.parts[0]
+            self.ws = api.dora_workspace(m, q.k, q.n, q.r_max, device=dev)
+        else:
+            self.ws = api.workspace(*ws_need[1], device=dev)
 
     def _fwd(self, d):
         api, q, s = self.api, d["part"], self.stream
-        if q.single:
+        if q.mag is not None:
+            a = d["adapters"][0]
+            api.dora_fwd(d["X"], d["W"], a.A, a.B, d["mag"], d["wn2"], a.alpha, a.p, q.seed, Y=d["Y"],
+                         S_saved=d["S"], g_saved=d["g"], mask_bits=d["M"], ws=self.ws, stream=s)
+        elif q.single:
             a = d["adapters"][0]
             api.lora_fwd(d["X"], d["W"], a.A, a.B, a.alpha, a.p, q.seed, Y=d["Y"], S_saved=d["S"], ws=self.ws,
                          stream=s)
@@ -531,7 +564,11 @@ class DeviceProblem:
 
     def _bwd(self, d):
         api, q, s = self.api, d["part"], self.stream
-        if q.single:
+        if q.mag is not None:
+            a = d["adapters"][0]
+            api.dora_bwd(d["dY"], d["X"], d["W"], a.A, a.B, d["S"], d["Y"], d["mag"], d["g"], a.alpha, a.p, q.seed,
+                         dX=d["dX"], dA=a.dA, dB=a.dB, dmag=d["dmag"], dZ=d["dZ"], ws=self.ws, stream=s)
+        elif q.single:
             a = d["adapters"][0]
             api.lora_bwd(d["dY"], d["X"], d["W"], a.A, a.B, d["S"], a.alpha, a.p, q.seed, dX=d["dX"], dA=a.dA,
                          dB=a.dB, ws=self.ws, stream=s)
@@ -566,6 +603,8 @@ class DeviceProblem:
             out += [d["Y"], d["dX"]]
             for a in d["adapters"]:
                 out += [a.dA, a.dB]
+            if "dmag" in d:
+                out.append(d["dmag"])
         return out
 
     def status(self) -> int:
@@ -816,7 +855,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, GREEDY, LAYER])
+    ap.add_argument("--workload", default="llama8b_up", choices=sorted(synth.WORKLOADS) + [MULTI, GREEDY, LAYER, DORA])
     ap.add_argument("--m", type=int, default=None,
                     help="override the workload's token count (padded rows for the packed workload)")
     ap.add_argument("--r", type=int, default=None, help="override the rank of a single-adapter workload")
