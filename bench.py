@@ -553,7 +553,7 @@ class DeviceProblem:
         if q.mag is not None:
             a = d["adapters"][0]
             api.dora_fwd(d["X"], d["W"], a.A, a.B, d["mag"], d["wn2"], a.alpha, a.p, q.seed, Y=d["Y"],
-                         S_saved=d["S"], g_saved=d["g"], mask_bits=d["M"], ws=self.ws, stream=s)
+                         S_saved=d["S"], g_saved=d["g"], ws=self.ws, stream=s)
         elif q.single:
             a = d["adapters"][0]
             api.lora_fwd(d["X"], d["W"], a.A, a.B, a.alpha, a.p, q.seed, Y=d["Y"], S_saved=d["S"], ws=self.ws,
