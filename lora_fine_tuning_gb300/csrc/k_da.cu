@@ -6,7 +6,9 @@
 // Each unit is (adapter a, 128-feature block, one of a's 128-row tiles): two
 // TMA boxes of X (128 tokens x 64 features, 128B swizzle) plus the tile's dSq
 // rows.  Warps 2..9 zero the dropped X elements in shared memory (Philox,
-// exactly as the forward), warp 1 issues tcgen05.mma with both operands
+// exactly as the forward) in two groups of four warps that take alternate
+// stages, a thread one token row of its stage (sixteen independent Philox
+// calls, eight at a time), warp 1 issues tcgen05.mma with both operands
 // MN-major (M = 128 features, N = rank, K = 128 tokens) accumulating over a
 // CTA's run of tiles of one (adapter, feature block), and the run's partial is
 // added into the adapter's fp32 accumulator with vector reductions.
@@ -19,11 +21,14 @@ namespace lora {
 
 namespace {
 
-constexpr int kMaskWarps = 8;                      // warps 2.. mask (2..5 also epilogue)
+constexpr int kMaskWarps = 8;                      // warps 2..9 mask, and run the epilogue
 constexpr int kMaskThreads = 32 * kMaskWarps;
 constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
-constexpr int kParts = kMaskThreads / 128;         // mask threads per token row
-constexpr int kChunks = 16 / kParts;               // 16-byte chunks (of the row's two boxes) per thread
+constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
+constexpr int kGroups = kMaskWarps / 4;            // mask groups, taking stages in turn
+constexpr int kChunks = 16;                        // 16-byte chunks of a token row (two 64-feature boxes)
+constexpr int kBatch = 8;                          // Philox calls computed before their chunks are masked
+static_assert(kGroupThreads == 128, "a group is four warps: one thread per token row, one warp per TMEM lane quadrant");
 constexpr uint32_t kXBytes = 2u * 128u * 128u;   // 128 tokens x 128 features
 
 struct DaUnit {
@@ -83,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&masked[s], kMaskThreads);
+            mbar_init(&masked[s], kGroupThreads);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -184,13 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // mask warps: thread -> (row, part) walks kChunks of the row's 16
-        // chunks (8 per 64-feature box).  Warps 2..5 also run the epilogue
-        // (TMEM lane quadrant = warp % 4).
+        // mask warps: group g takes the units u0 + g, u0 + g + kGroups, ...; in
+        // it thread -> token row covers the row's 16 chunks (8 per 64-feature
+        // box).  The group that masks a run's last stage also runs its epilogue
+        // (TMEM lane quadrant = warp % 4; each group has one warp per quadrant).
         const int mt = threadIdx.x - 64;
+        const int group = mt / kGroupThreads;
         const int row = mt & 127;
-        const int part = mt >> 7;
-        const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         uint32_t prow_t = 0xFFFFFFFFu;   // row whose Philox words are in prow
@@ -198,10 +203,18 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
+        int turn = 0;                    // whose unit this is: the group with turn == group
         DaUnit d = da_unit(u0, p);
         for (int64_t u = u0; u < u1; ++u, da_next(d, p)) {
-            const AdapterDev ad = p.rt.ad[d.a];
             const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
+            const bool mine = turn == group;
+            if (++turn == kGroups) turn = 0;
+            if (!mine) {
+                if (last) ++use;
+                if (++s == S) { s = 0; ph ^= 1u; }
+                continue;
+            }
+            const AdapterDev ad = p.rt.ad[d.a];
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (ad.T != 0u) {
@@ -214,21 +227,26 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 const KeepTest kt = keep_test(ad.T);
 #pragma unroll
-                for (int i = 0; i < kChunks; ++i) {
-                    const int cc = part * kChunks + i;          // chunk of the row: box cc / 8, chunk cc % 8
-                    const uint4 wv = philox_10_row(prow, g0 + cc, keys);
-                    const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
-                    uint4 v = lds128(addr);
-                    v.x = apply_keep_fast(v.x, wv.x, kt);
-                    v.y = apply_keep_fast(v.y, wv.y, kt);
-                    v.z = apply_keep_fast(v.z, wv.z, kt);
-                    v.w = apply_keep_fast(v.w, wv.w, kt);
-                    sts128(addr, v);
+                for (int c0 = 0; c0 < kChunks; c0 += kBatch) {
+                    uint4 wv[kBatch];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) wv[i] = philox_10_row(prow, g0 + c0 + i, keys);
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int cc = c0 + i;                      // chunk of the row: box cc / 8, chunk cc % 8
+                        const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
+                        uint4 v = lds128(addr);
+                        v.x = apply_keep_fast(v.x, wv[i].x, kt);
+                        v.y = apply_keep_fast(v.y, wv[i].y, kt);
+                        v.z = apply_keep_fast(v.z, wv[i].z, kt);
+                        v.w = apply_keep_fast(v.w, wv[i].w, kt);
+                        sts128(addr, v);
+                    }
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&masked[s]);
-            if (last && epilogue) {
+            if (last) {
                 const uint32_t b = use & 1u;
                 ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -250,8 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
+                ++use;
             }
-            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }

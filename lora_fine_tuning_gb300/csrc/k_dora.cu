@@ -64,9 +64,13 @@ __global__ void __launch_bounds__(256) dora_gram_kernel(const uint16_t* __restri
     }
 }
 
-// g_j = mag_j / sqrt(||W_j||^2 + 2 alpha B_j . U_j + alpha^2 B_j^T G B_j), one thread per column; U's row j
-// is cleared (the workspace is zero between calls).  Dynamic shared memory: G (r x r) and the block's
-// 256 columns of B (r x 256), both fp32.
+// g_j = mag_j / sqrt(||W_j||^2 + 2 alpha B_j . U_j + alpha^2 B_j^T G B_j).  A block of 256 threads takes
+// kScaleCols columns, eight threads per column: thread `part` of column j sums the terms c = part, part + 8,
+// ... of  B_cj U_jc  and  B_cj (G B_j)_c , and the eight partial sums meet by warp shuffles.  U's row j is
+// cleared (the workspace is zero between calls).  Dynamic shared memory: G (r x r) and the block's columns
+// of B (r x kScaleCols), both fp32.
+constexpr int kScaleCols = 32;
+
 __global__ void __launch_bounds__(256) dora_scale_kernel(float* __restrict__ U, int rpad, const uint16_t* __restrict__ B,
                                                          const float* __restrict__ G, int r, const float* __restrict__ wn2,
                                                          const float* __restrict__ mag, float alpha, int64_t n,
@@ -75,29 +79,47 @@ __global__ void __launch_bounds__(256) dora_scale_kernel(float* __restrict__ U, 
     pdl_trigger();
     extern __shared__ float sh[];
     float* g_s = sh;              // r x r
-    float* b_s = sh + r * r;      // r x 256 (column-local)
-    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 256;
+    float* b_s = sh + r * r;      // r x kScaleCols (column-local)
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kScaleCols;
     for (int i = threadIdx.x; i < r * r; i += blockDim.x) g_s[i] = G[i];
-    for (int i = threadIdx.x; i < r * 256; i += blockDim.x) {
-        const int c = i >> 8, jj = i & 255;
+    for (int i = threadIdx.x; i < r * kScaleCols; i += blockDim.x) {
+        const int c = i / kScaleCols, jj = i - c * kScaleCols;
         b_s[i] = (j0 + jj < n) ? bf16_to_f32(B[c * n + j0 + jj]) : 0.f;
     }
     __syncthreads();
-    const int jj = threadIdx.x;
+    const int jj = threadIdx.x >> 3;
+    const int part = threadIdx.x & 7;
     const int64_t j = j0 + jj;
-    if (j >= n) return;
-    float* u = U + j * rpad;
+    const bool valid = j < n;   // all eight threads of a column agree
     float cross = 0.f, quad = 0.f;
-    for (int c = 0; c < r; ++c) {
-        const float bc = b_s[c * 256 + jj];
-        cross = fmaf(bc, u[c], cross);
-        float gb = 0.f;
-        for (int d = 0; d < r; ++d) gb = fmaf(g_s[c * r + d], b_s[d * 256 + jj], gb);
-        quad = fmaf(bc, gb, quad);
+    if (valid) {
+        float* u = U + j * rpad;
+        for (int c = part; c < r; c += 8) {
+            const float bc = b_s[c * kScaleCols + jj];
+            cross = fmaf(bc, u[c], cross);
+            const float* gc = g_s + c * r;
+            float gb0 = 0.f, gb1 = 0.f;
+            int d = 0;
+            for (; d + 1 < r; d += 2) {
+                gb0 = fmaf(gc[d], b_s[d * kScaleCols + jj], gb0);
+                gb1 = fmaf(gc[d + 1], b_s[(d + 1) * kScaleCols + jj], gb1);
+            }
+            if (d < r) gb0 = fmaf(gc[d], b_s[d * kScaleCols + jj], gb0);
+            quad = fmaf(bc, gb0 + gb1, quad);
+        }
     }
-    for (int c = 0; c < rpad; c += 4) st_zero_f4(u + c);
-    const float norm2 = wn2[j] + 2.f * alpha * cross + alpha * alpha * quad;
-    g_out[j] = mag[j] * rsqrtf(fmaxf(norm2, 1e-30f));
+    __syncwarp();   // the column's eight threads have read U's row before any of it is cleared
+    if (valid)
+        for (int c = 4 * part; c < rpad; c += 32) st_zero_f4(U + j * rpad + c);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        cross += __shfl_xor_sync(0xFFFFFFFFu, cross, o);
+        quad += __shfl_xor_sync(0xFFFFFFFFu, quad, o);
+    }
+    if (valid && part == 0) {
+        const float norm2 = wn2[j] + 2.f * alpha * cross + alpha * alpha * quad;
+        g_out[j] = mag[j] * rsqrtf(fmaxf(norm2, 1e-30f));
+    }
 }
 
 // dZ = dY * g (bf16) and dmag_acc_j += sum_t dY[t, j] Y[t, j] over this block's rows; eight columns per
@@ -152,7 +174,7 @@ __global__ void __launch_bounds__(256) dora_dmag_kernel(float* __restrict__ dmag
 
 cudaError_t dora_configure() {
     return cudaFuncSetAttribute(dora_scale_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (kMaxRank * kMaxRank + kMaxRank * 256) * 4);
+                                (kMaxRank * kMaxRank + kMaxRank * kScaleCols) * 4);
 }
 
 cudaError_t launch_dora_norm2(const uint16_t* W, int64_t k, int64_t n, float* out, int sms, cudaStream_t stream) {
@@ -170,8 +192,8 @@ cudaError_t launch_dora_gram(const uint16_t* A, int64_t k, int r, float* G, cuda
 
 cudaError_t launch_dora_scale(float* U, int rpad, const uint16_t* B, const float* G, int r, const float* wn2,
                               const float* mag, float alpha, int64_t n, float* g_out, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(r * r + r * 256) * 4;
-    return launch_pdl(dora_scale_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), smem, stream, U,
+    const size_t smem = static_cast<size_t>(r * r + r * kScaleCols) * 4;
+    return launch_pdl(dora_scale_kernel, dim3(static_cast<unsigned>((n + kScaleCols - 1) / kScaleCols)), dim3(256), smem, stream, U,
                       rpad, B, G, r, wn2, mag, alpha, n, g_out);
 }
 

@@ -7,12 +7,16 @@
 //    64-row block of A_a into a ring of shared-memory stages;
 //  - warps 2..9 regenerate the keep mask with Philox4x32-10 and zero the
 //    dropped elements in place (16 bytes = 8 features = one Philox call per
-//    access; each thread walks one row, so the counter's row word is shared),
-//    then hand the stage to the MMA warp;
+//    access), then hand the stage to the MMA warp.  They form two groups of
+//    four warps that take alternate stages, and a thread owns one whole row
+//    of its stage: eight independent Philox calls per thread and stage, with
+//    the counter's row word shared.  The Philox rounds are a chain of
+//    dependent multiplies, so it is the independent calls in flight per
+//    scheduler that set the mask rate;
 //  - warp 1 issues tcgen05.mma (M = 128 tokens, N = rank, K = 64 per stage)
 //    into a double-buffered TMEM accumulator;
-//  - at the end of each tile range, warps 2..5 read TMEM and add the fp32
-//    partial into S_acc with vector reductions (ranges of one tile may be
+//  - at the end of each tile range, the group that masked its last stage
+//    reads TMEM and adds the fp32 partial into S_acc with vector reductions (ranges of one tile may be
 //    split over CTAs: units are spread evenly, stream-K style).
 // finalize_s then applies alpha/(1-p), writes S' in bf16 and clears S_acc,
 // which starts every call at zero.
@@ -23,11 +27,14 @@ namespace lora {
 
 namespace {
 
-constexpr int kMaskWarps = 8;                      // warps 2.. mask (2..5 also epilogue)
+constexpr int kMaskWarps = 8;                      // warps 2..9 mask, and run the epilogue
 constexpr int kMaskThreads = 32 * kMaskWarps;
 constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
-constexpr int kParts = kMaskThreads / 128;         // mask threads per tile row
+constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
+constexpr int kGroups = kMaskWarps / 4;            // mask groups, taking stages in turn
+constexpr int kParts = kGroupThreads / 128;        // group threads per tile row
 constexpr int kChunks = 8 / kParts;                // 16-byte chunks (8 features) per thread and stage
+static_assert(kGroupThreads == 128, "a group is four warps: one thread per tile row, one warp per TMEM lane quadrant");
 constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16; then 64 rows of A (rpad_max x 2 bytes each)
 
 __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_constant__ DownParams p) {
@@ -52,12 +59,12 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&masked[s], kMaskThreads);
+            mbar_init(&masked[s], kGroupThreads);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 128);
+            mbar_init(&acc_empty[b], kGroupThreads);
         }
         mbar_init(drain, 1);
         abort_flag = 0;
@@ -158,14 +165,14 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
     } else {
-        // mask warps: thread -> (row, part) covers the kChunks 16-byte chunks
-        // [kChunks*part, kChunks*part + kChunks) of one row, so the Philox
-        // counter word is the row for all of them.  Warps 2..5 also run the
-        // epilogue (TMEM lane quadrant = warp % 4).
+        // mask warps: group g takes the units u0 + g, u0 + g + kGroups, ...; in
+        // it thread -> row covers the row's kChunks 16-byte chunks, so the
+        // Philox counter word is the row for all of them.  The group that
+        // masks a tile range's last stage also runs its epilogue (TMEM lane
+        // quadrant = warp % 4; each group has one warp per quadrant).
         const int mt = threadIdx.x - 64;
+        const int group = mt / kGroupThreads;
         const int row = mt & 127;
-        const int part = mt >> 7;
-        const bool epilogue = warp < 6;
         const int quad = warp & 3;
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         uint32_t prow_t = 0xFFFFFFFFu;   // row whose Philox words are in prow
@@ -173,13 +180,21 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
         int s = 0;
         uint32_t ph = 0;
         uint32_t use = 0;
+        int turn = 0;                    // whose unit this is: the group with turn == group
         TileBlockIter it(u0, p.nkb, p.rt);
         for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
             const int kb = it.blk;
+            const bool last = (u == u1 - 1) || kb == p.nkb - 1;
+            const bool mine = turn == group;
+            if (++turn == kGroups) turn = 0;
+            if (!mine) {
+                if (last) ++use;
+                if (++s == S) { s = 0; ph ^= 1u; }
+                continue;
+            }
             const int tile = it.tile;
             const int a = it.a;
             const uint32_t T = p.rt.ad[a].T;
-            const bool last = (u == u1 - 1) || kb == p.nkb - 1;
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             if (T != 0u || p.mask_bits != nullptr) {
@@ -192,13 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 uint4 wv[kChunks];
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i)
-                    wv[i] = philox_10_row(prow, static_cast<uint32_t>(kb * 8 + part * kChunks + i), keys);
+                    wv[i] = philox_10_row(prow, static_cast<uint32_t>(kb * 8 + i), keys);
                 if (T != 0u) {
                     const KeepTest kt = keep_test(T);
 #pragma unroll
                     for (int i = 0; i < kChunks; ++i) {
-                        const int c16 = part * kChunks + i;
-                        const uint32_t addr = xrow + ((c16 ^ (row & 7)) << 4);
+                        const uint32_t addr = xrow + ((i ^ (row & 7)) << 4);
                         uint4 v = lds128(addr);
                         v.x = apply_keep_fast(v.x, wv[i].x, kt);
                         v.y = apply_keep_fast(v.y, wv[i].y, kt);
@@ -210,14 +224,14 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 if (p.mask_bits != nullptr && t < p.m) {
 #pragma unroll
                     for (int i = 0; i < kChunks; ++i) {
-                        const int64_t g = static_cast<int64_t>(kb) * 8 + part * kChunks + i;
+                        const int64_t g = static_cast<int64_t>(kb) * 8 + i;
                         if (g * 8 < p.k) p.mask_bits[t * (p.k >> 3) + g] = static_cast<uint8_t>(keep_byte(wv[i], T));
                     }
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&masked[s]);
-            if (last && epilogue) {
+            if (last) {
                 const uint32_t b = use & 1u;
                 ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -240,8 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
+                ++use;
             }
-            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }
