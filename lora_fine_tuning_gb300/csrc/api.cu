@@ -24,6 +24,11 @@ struct DeviceState {
     bool ready = false;
     lora_status status = LORA_OK;
     int sms = 0;
+    // The backward's dA pass runs on `side`, forked from and joined back to the
+    // caller's stream, so that it can use the SMs the dX GEMM's last wave of
+    // tiles leaves idle.
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mu;
@@ -100,7 +105,10 @@ lora_status device_setup(int* sms_out) {
             d.sms = sms;
             if (!cuda_ok(down_configure()) || !cuda_ok(gemm2_configure()) ||
                 !cuda_ok(dsdb_configure()) ||
-                !cuda_ok(da_configure()) || !cuda_ok(dora_configure()))
+                !cuda_ok(da_configure()) || !cuda_ok(dora_configure()) ||
+                !cuda_ok(cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking)) ||
+                !cuda_ok(cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming)) ||
+                !cuda_ok(cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming)))
                 d.status = LORA_ECUDA;
         }
         if (d.status == LORA_OK && g_encode == nullptr) {
@@ -118,6 +126,16 @@ lora_status device_setup(int* sms_out) {
     if (d.status != LORA_OK) return d.status;
     *sms_out = d.sms;
     return LORA_OK;
+}
+
+// The current device's side stream and its fork / join events (device_setup has run).
+void side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const DeviceState& d = g_dev[dev];
+    *side = d.side;
+    *fork = d.fork;
+    *join = d.join;
 }
 
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
@@ -441,6 +459,17 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, c.sms, c.stream); }));
     }
 
+    // dA only needs dSq (written above) and X, not dX: it is forked onto the side stream, launched after
+    // the dX GEMM so that the GEMM's CTAs take the SMs first, and joined back before finalize_da.
+    const bool fork_da = nad > 0 && c.rt.n_active > 0;
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    if (fork_da) {
+        side_stream(&side, &ev_fork, &ev_join);
+        LORA_CUDA(cudaEventRecord(ev_fork, c.stream));
+        LORA_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
+    }
+
     if (m > 0) {
         static GemmParams g;
         std::memset(&g, 0, sizeof(g));
@@ -466,7 +495,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, kBwdPairBN, c.sms, c.stream); }));
     }
 
-    if (nad > 0 && c.rt.n_active > 0) {
+    if (fork_da) {
         static DaParams p;
         std::memset(&p, 0, sizeof(p));
         if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
@@ -498,7 +527,9 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.stage_bytes = p.off_d + 256 * rpm;
         p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-        LORA_CUDA(timed(kDa, c.stream, [&] { return launch_da(p, grid, c.stream); }));
+        LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side); }));
+        LORA_CUDA(cudaEventRecord(ev_join, side));
+        LORA_CUDA(cudaStreamWaitEvent(c.stream, ev_join, 0));
         LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(p, c.sms, c.stream); }));
     }
     return LORA_OK;
