@@ -531,6 +531,7 @@ class DeviceProblem:
                      W=weight(q.W), Y=torch.empty((m, q.n), dtype=bf, device=dev),
                      dX=torch.empty((m, q.k), dtype=bf, device=dev),
                      S=torch.empty((m, q.r_max), dtype=bf, device=dev),
+                     M=torch.empty((m, q.k // 8), dtype=torch.uint8, device=dev),   # keep bits, fwd -> bwd
                      adapters=[api.Adapter(A=weight(A), B=weight(B), alpha=a, p=p,
                                            dA=torch.empty((q.k, r), dtype=bf, device=dev),
                                            dB=torch.empty((r, q.n), dtype=bf, device=dev))
@@ -556,28 +557,29 @@ class DeviceProblem:
         if q.mag is not None:
             a = d["adapters"][0]
             api.dora_fwd(d["X"], d["W"], a.A, a.B, d["mag"], d["wn2"], a.alpha, a.p, q.seed, Y=d["Y"],
-                         S_saved=d["S"], g_saved=d["g"], ws=self.ws, stream=s)
+                         S_saved=d["S"], g_saved=d["g"], mask_bits=d["M"], ws=self.ws, stream=s)
         elif q.single:
             a = d["adapters"][0]
-            api.lora_fwd(d["X"], d["W"], a.A, a.B, a.alpha, a.p, q.seed, Y=d["Y"], S_saved=d["S"], ws=self.ws,
-                         stream=s)
+            api.lora_fwd(d["X"], d["W"], a.A, a.B, a.alpha, a.p, q.seed, Y=d["Y"], S_saved=d["S"],
+                         mask_bits=d["M"], ws=self.ws, stream=s)
         else:
             api.multi_lora_fwd(d["X"], d["W"], d["adapters"], q.segments, q.seed, Y=d["Y"], S_saved=d["S"],
-                               ws=self.ws, stream=s)
+                               mask_bits=d["M"], ws=self.ws, stream=s)
 
     def _bwd(self, d):
         api, q, s = self.api, d["part"], self.stream
         if q.mag is not None:
             a = d["adapters"][0]
             api.dora_bwd(d["dY"], d["X"], d["W"], a.A, a.B, d["S"], d["Y"], d["mag"], d["g"], a.alpha, a.p, q.seed,
-                         dX=d["dX"], dA=a.dA, dB=a.dB, dmag=d["dmag"], dZ=d["dZ"], ws=self.ws, stream=s)
+                         dX=d["dX"], dA=a.dA, dB=a.dB, dmag=d["dmag"], dZ=d["dZ"], ws=self.ws, stream=s,
+                         mask_bits=d["M"])
         elif q.single:
             a = d["adapters"][0]
             api.lora_bwd(d["dY"], d["X"], d["W"], a.A, a.B, d["S"], a.alpha, a.p, q.seed, dX=d["dX"], dA=a.dA,
-                         dB=a.dB, ws=self.ws, stream=s)
+                         dB=a.dB, ws=self.ws, stream=s, mask_bits=d["M"])
         else:
             api.multi_lora_bwd(d["dY"], d["X"], d["W"], d["adapters"], q.segments, q.seed, d["S"], dX=d["dX"],
-                               ws=self.ws, stream=s)
+                               ws=self.ws, stream=s, mask_bits=d["M"])
 
     def step(self):
         for d in self.parts:
@@ -845,7 +847,8 @@ def run_native(args):
 
     config = {"workload": wl.describe(), "m": wl.m, "k": [q.k for q in wl.parts], "n": [q.n for q in wl.parts],
               "r": [[r for r, _, _ in q.specs] for q in wl.parts], "tokens_per_step": wl.tokens,
-              "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU", "l2": l2_note}
+              "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU", "l2": l2_note,
+              "saved_for_backward": "S_saved and the keep bits (m x k/8 bytes) written by the forward"}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, Llama-shaped)", "config": config,

@@ -113,11 +113,16 @@ lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
 /* Backward, one adapter, W frozen.  Inputs: dY (m x n), the forward's X, W,
  * A, B, S_saved and the same alpha, p, seed.  Writes
  *   dX = dY W^T + (D q) * (dS A^T),  dA = X_hat^T dS,  dB = alpha S^T dY,
- * with dS = alpha dY B^T (article section 4.1, backward ③ and ⑤). */
+ * with dS = alpha dY B^T (article section 4.1, backward ③ and ⑤).
+ * mask_bits (optional, 16-byte aligned): the keep bits the forward wrote with
+ * the same X, seed and p.  When given, the backward reads the mask instead of
+ * regenerating it (the results are the same; the dX GEMM uses them when
+ * k % 32 == 0, the dA pass when k % 128 == 0).  NULL: the mask is
+ * regenerated from the seed. */
 lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
-                     const lora_bf16* B, const lora_bf16* S_saved, float alpha, float p, uint64_t seed,
-                     int64_t m, int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB,
-                     void* workspace, size_t workspace_bytes, void* stream);
+                     const lora_bf16* B, const lora_bf16* S_saved, const uint8_t* mask_bits, float alpha, float p,
+                     uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA,
+                     lora_bf16* dB, void* workspace, size_t workspace_bytes, void* stream);
 
 /* Forward, packed multi-adapter batch.  `adapters` and `segments` are HOST
  * arrays, read before the call returns.  S_saved is m x s_ld with
@@ -131,11 +136,12 @@ lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_ad
                            void* workspace, size_t workspace_bytes, void* stream);
 
 /* Backward of multi_lora_fwd.  Writes dX (m x k) and every adapter's dA_i,
- * dB_i (adapters without rows get zeros). */
+ * dB_i (adapters without rows get zeros).  mask_bits: optional, as lora_bwd
+ * (the bits multi_lora_fwd wrote for the same batch). */
 lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters,
                            int32_t n_adapters, const lora_segment* segments, int32_t n_segments, uint64_t seed,
-                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX,
-                           void* workspace, size_t workspace_bytes, void* stream);
+                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, const uint8_t* mask_bits,
+                           lora_bf16* dX, void* workspace, size_t workspace_bytes, void* stream);
 
 /* DoRA ("Scaling DoRA", paper.rainbus.top): the adapted weight split into a
  * magnitude per output feature and a direction,
@@ -169,10 +175,12 @@ lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
  * fix no backward): dZ = dY * g feeds the LoRA backward, giving dX, dA, dB;
  * dmag_j = sum_t dY[t, j] Y[t, j] / mag_j (= sum_t dY Z / ||.||_j).  Inputs
  * are the forward's X, W, A, B, S_saved, Y, mag, g_saved and the same alpha,
- * p, seed.  dZ: caller scratch of m x n bf16 (16-byte aligned; its contents
- * before and after the call do not matter). */
+ * p, seed.  mask_bits: optional, as lora_bwd (the bits dora_fwd wrote).
+ * dZ: caller scratch of m x n bf16 (16-byte aligned; its contents before and
+ * after the call do not matter). */
 lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
-                     const lora_bf16* B, const lora_bf16* S_saved, const lora_bf16* Y, const float* mag,
+                     const lora_bf16* B, const lora_bf16* S_saved, const uint8_t* mask_bits, const lora_bf16* Y,
+                     const float* mag,
                      const float* g_saved, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
                      int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, float* dmag, lora_bf16* dZ,
                      void* workspace, size_t workspace_bytes, void* stream);

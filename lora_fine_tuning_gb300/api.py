@@ -73,8 +73,9 @@ def lora_fwd(X, W, A, B, alpha: float, p: float, seed: int, *, Y=None, S_saved=N
 
 
 def lora_bwd(dY, X, W, A, B, S_saved, alpha: float, p: float, seed: int, *, dX=None, dA=None, dB=None, ws=None,
-             stream=None):
-    """Gradients of lora_fwd with W frozen.  Returns (dX, dA, dB)."""
+             stream=None, mask_bits=None):
+    """Gradients of lora_fwd with W frozen.  Returns (dX, dA, dB).  mask_bits: optional, the keep bits
+    lora_fwd wrote for the same inputs (read instead of regenerating the mask)."""
     m, k = X.shape
     n = W.shape[1]
     r = A.shape[1]
@@ -84,8 +85,10 @@ def lora_bwd(dY, X, W, A, B, S_saved, alpha: float, p: float, seed: int, *, dX=N
     dX = dX if dX is not None else torch.empty((m, k), dtype=torch.bfloat16, device=X.device)
     dA = dA if dA is not None else torch.empty((k, r), dtype=torch.bfloat16, device=X.device)
     dB = dB if dB is not None else torch.empty((r, n), dtype=torch.bfloat16, device=X.device)
+    _check_bits(mask_bits, m, k)
     ws = ws if ws is not None else workspace(m, k, n, r)
-    st = native.lib().lora_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(S_saved), float(alpha), float(p),
+    st = native.lib().lora_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(S_saved), _ptr(mask_bits),
+                               float(alpha), float(p),
                                int(seed) & (2**64 - 1), m, k, n, r, _ptr(dX), _ptr(dA), _ptr(dB), _ptr(ws),
                                ws.numel(), _stream(stream))
     native.check("lora_bwd", st)
@@ -148,8 +151,9 @@ def multi_lora_fwd(X, W, adapters: Sequence[Adapter], segments, seed: int, *, Y=
 
 
 def multi_lora_bwd(dY, X, W, adapters: Sequence[Adapter], segments, seed: int, S_saved, *, dX=None, ws=None,
-                   stream=None):
-    """Packed multi-adapter backward.  Fills each adapter's dA / dB (allocated if missing); returns dX."""
+                   stream=None, mask_bits=None):
+    """Packed multi-adapter backward.  Fills each adapter's dA / dB (allocated if missing); returns dX.
+    mask_bits: optional, the keep bits multi_lora_fwd wrote for the same batch."""
     m, k = X.shape
     n = W.shape[1]
     _check_bf16("dY", dY, (m, n))
@@ -165,9 +169,10 @@ def multi_lora_bwd(dY, X, W, adapters: Sequence[Adapter], segments, seed: int, S
     ws = ws if ws is not None else workspace(m, k, n, max(s_ld, 8), max(1, len(adapters)))
     seg = native.segments_array(segments)
     ad = _adapter_array(adapters, True)
+    _check_bits(mask_bits, m, k)
     st = native.lib().multi_lora_bwd(_ptr(dY), _ptr(X), _ptr(W), ad, len(adapters), seg, len(segments),
-                                     int(seed) & (2**64 - 1), m, k, n, _ptr(S_saved), _ptr(dX), _ptr(ws), ws.numel(),
-                                     _stream(stream))
+                                     int(seed) & (2**64 - 1), m, k, n, _ptr(S_saved), _ptr(mask_bits), _ptr(dX),
+                                     _ptr(ws), ws.numel(), _stream(stream))
     native.check("multi_lora_bwd", st)
     return dX
 
@@ -184,6 +189,14 @@ def dora_workspace(m: int, k: int, n: int, r: int, device=None) -> torch.Tensor:
         ws = torch.zeros(max(size, 256), dtype=torch.uint8, device=device)
         _DORA_WS[device.index] = ws
     return ws
+
+
+def _check_bits(t, m: int, k: int) -> None:
+    """The forward's keep bits handed to a backward: m x k/8 bytes, contiguous, on the device."""
+    if t is None:
+        return
+    if t.dtype != torch.uint8 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (m, k // 8):
+        raise ValueError(f"mask_bits must be a contiguous CUDA uint8 tensor of shape {(m, k // 8)}")
 
 
 def _check_f32(name: str, t: torch.Tensor, n: int) -> None:
@@ -225,9 +238,9 @@ def dora_fwd(X, W, A, B, mag, w_norm2, alpha: float, p: float, seed: int, *, Y=N
 
 
 def dora_bwd(dY, X, W, A, B, S_saved, Y, mag, g_saved, alpha: float, p: float, seed: int, *, dX=None, dA=None,
-             dB=None, dmag=None, dZ=None, ws=None, stream=None):
+             dB=None, dmag=None, dZ=None, ws=None, stream=None, mask_bits=None):
     """DoRA backward with the column norm held constant.  Returns (dX, dA, dB, dmag).
-    dZ: m x n bf16 scratch (allocated if not given)."""
+    dZ: m x n bf16 scratch (allocated if not given).  mask_bits: optional, the keep bits dora_fwd wrote."""
     m, k = X.shape
     n = W.shape[1]
     r = A.shape[1]
@@ -242,8 +255,10 @@ def dora_bwd(dY, X, W, A, B, S_saved, Y, mag, g_saved, alpha: float, p: float, s
     dmag = dmag if dmag is not None else torch.empty(n, dtype=torch.float32, device=X.device)
     dZ = dZ if dZ is not None else torch.empty((m, n), dtype=torch.bfloat16, device=X.device)
     _check_bf16("dZ", dZ, (m, n))
+    _check_bits(mask_bits, m, k)
     ws = ws if ws is not None else dora_workspace(m, k, n, r)
-    st = native.lib().dora_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(S_saved), _ptr(Y), _ptr(mag),
+    st = native.lib().dora_bwd(_ptr(dY), _ptr(X), _ptr(W), _ptr(A), _ptr(B), _ptr(S_saved), _ptr(mask_bits),
+                               _ptr(Y), _ptr(mag),
                                _ptr(g_saved), float(alpha), float(p), int(seed) & (2**64 - 1), m, k, n, r, _ptr(dX),
                                _ptr(dA), _ptr(dB), _ptr(dmag), _ptr(dZ), _ptr(ws), ws.numel(), _stream(stream))
     native.check("dora_bwd", st)

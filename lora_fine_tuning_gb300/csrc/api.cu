@@ -153,6 +153,20 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer
     return r == CUDA_SUCCESS;
 }
 
+// 2-D byte tensor map (keep bits): `inner` bytes per row, `outer` rows, `ld` bytes between rows, no swizzle.
+bool make_map_u8(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                 uint32_t box_outer) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) g_last_error = "cuTensorMapEncodeTiled rejected a tensor map";
+    return r == CUDA_SUCCESS;
+}
+
 CUtensorMapSwizzle rank_swizzle_host(int rpad) {
     return rpad <= 16 ? CU_TENSOR_MAP_SWIZZLE_32B : (rpad <= 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
 }
@@ -410,7 +424,8 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
 }
 
 lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const uint16_t* W, const lora_adapter* ads,
-                    uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, uint16_t* dX) {
+                    uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, const uint8_t* mask_bits,
+                    uint16_t* dX) {
     const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
     const int nad = c.rt.n_adapters;
     uint16_t* dsq = reinterpret_cast<uint16_t*>(c.ws + c.L.dsq);
@@ -492,6 +507,8 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         g.nkb = static_cast<int32_t>((n + 63) / 64);
         g.seed_lo = seed_lo;
         g.seed_hi = seed_hi;
+        // the forward's keep bits, when given, replace the epilogue's Philox (whole 32-bit words per row)
+        g.keep_bits = (mask_bits != nullptr && k % 32 == 0) ? mask_bits : nullptr;
         LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, kBwdPairBN, c.sms, c.stream); }));
     }
 
@@ -525,6 +542,13 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         const uint32_t rpm = static_cast<uint32_t>(c.rt.rpad_max);
         p.off_d = 32768;
         p.stage_bytes = p.off_d + 256 * rpm;
+        // the forward's keep bits, when given, come with each X stage (16 bytes a row; rows of whole 16 bytes)
+        p.use_bits = (mask_bits != nullptr && k % 128 == 0) ? 1 : 0;
+        if (p.use_bits) {
+            if (!make_map_u8(&p.mapBits, mask_bits, k / 8, m, k / 8, 16, 128)) return LORA_ECUDA;
+            p.off_bits = p.stage_bytes;
+            p.stage_bytes += 2048;
+        }
         p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side); }));
@@ -647,10 +671,11 @@ lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_ad
 
 lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters,
                            int32_t n_adapters, const lora_segment* segments, int32_t n_segments, uint64_t seed,
-                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, lora_bf16* dX, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           int64_t m, int64_t k, int64_t n, const lora_bf16* S_saved, const uint8_t* mask_bits,
+                           lora_bf16* dX, void* workspace, size_t workspace_bytes, void* stream) {
     if (!W || (m > 0 && (!X || !dY || !dX))) return LORA_EINVAL;
-    if (!aligned16(dY) || !aligned16(X) || !aligned16(W) || !aligned16(dX) || !aligned16(S_saved))
+    if (!aligned16(dY) || !aligned16(X) || !aligned16(W) || !aligned16(dX) || !aligned16(S_saved) ||
+        !aligned16(mask_bits))
         return LORA_EALIGN;
     if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
     std::lock_guard<std::mutex> lock(g_call_mu);
@@ -658,7 +683,7 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
     lora_status st = prepare(c, adapters, n_adapters, segments, n_segments, m, k, n, true, workspace,
                              workspace_bytes, stream);
     if (st) return st;
-    return run_bwd(c, dY, X, W, adapters, seed, m, k, n, S_saved, dX);
+    return run_bwd(c, dY, X, W, adapters, seed, m, k, n, S_saved, mask_bits, dX);
 }
 
 lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B, float alpha,
@@ -671,12 +696,12 @@ lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
 }
 
 lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
-                     const lora_bf16* B, const lora_bf16* S_saved, float alpha, float p, uint64_t seed, int64_t m,
-                     int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+                     const lora_bf16* B, const lora_bf16* S_saved, const uint8_t* mask_bits, float alpha, float p,
+                     uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r, lora_bf16* dX, lora_bf16* dA,
+                     lora_bf16* dB, void* workspace, size_t workspace_bytes, void* stream) {
     lora_adapter ad{r, alpha, p, A, B, dA, dB};
     lora_segment seg{0, m, 0, 0};
-    return multi_lora_bwd(dY, X, W, &ad, 1, &seg, m > 0 ? 1 : 0, seed, m, k, n, S_saved, dX, workspace,
+    return multi_lora_bwd(dY, X, W, &ad, 1, &seg, m > 0 ? 1 : 0, seed, m, k, n, S_saved, mask_bits, dX, workspace,
                           workspace_bytes, stream);
 }
 
@@ -855,14 +880,16 @@ lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
 }
 
 lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
-                     const lora_bf16* B, const lora_bf16* S_saved, const lora_bf16* Y, const float* mag,
+                     const lora_bf16* B, const lora_bf16* S_saved, const uint8_t* mask_bits, const lora_bf16* Y,
+                     const float* mag,
                      const float* g_saved, float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n,
                      int32_t r, lora_bf16* dX, lora_bf16* dA, lora_bf16* dB, float* dmag, lora_bf16* dZ,
                      void* workspace, size_t workspace_bytes, void* stream) {
     if (!W || !mag || !g_saved || !dmag || (m > 0 && (!X || !dY || !dX || !Y || !S_saved || !dZ)))
         return LORA_EINVAL;
     if (!aligned16(dY) || !aligned16(X) || !aligned16(W) || !aligned16(dX) || !aligned16(S_saved) ||
-        !aligned16(Y) || !aligned16(mag) || !aligned16(g_saved) || !aligned16(dmag) || !aligned16(dZ))
+        !aligned16(Y) || !aligned16(mag) || !aligned16(g_saved) || !aligned16(dmag) || !aligned16(dZ) ||
+        !aligned16(mask_bits))
         return LORA_EALIGN;
     lora_adapter ad{r, alpha, p, A, B, dA, dB};
     lora_segment seg{0, m, 0, 0};
@@ -876,7 +903,7 @@ lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
     if (m > 0)
         LORA_CUDA(timed(kDoraDz, c.stream, [&] { return launch_dora_dz(dY, Y, g_saved, m, n, dZ, dmag_acc, c.sms,
                                                                       c.stream); }));
-    st = run_bwd(c, dZ, X, W, &ad, seed, m, k, n, S_saved, dX);
+    st = run_bwd(c, dZ, X, W, &ad, seed, m, k, n, S_saved, mask_bits, dX);
     if (st) return st;
     LORA_CUDA(timed(kDoraDmag, c.stream, [&] { return launch_dora_dmag(dmag_acc, mag, n, dmag, c.stream); }));
     return LORA_OK;

@@ -371,6 +371,23 @@ __device__ __forceinline__ KeepTest keep_test(uint32_t T) {
     return KeepTest{(c & 0x7FFFu) * 0x10001u, (c & 0x8000u) * 0x10001u};
 }
 
+// The keep decisions of one Philox word as a carry: bit 15 set iff the low
+// lane is >= T, bit 31 iff the high lane is (see apply_keep_fast).
+__device__ __forceinline__ uint32_t keep_carry(uint32_t w, const KeepTest& kt) {
+    const uint32_t s = (w & 0x7FFF7FFFu) + kt.low;
+    return (w & kt.top) | (w & s) | (kt.top & s);
+}
+
+// AND mask of a packed bf16 pair from keep_carry: each carry bit spread over its lane.
+__device__ __forceinline__ uint32_t carry_mask(uint32_t carry) {
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(carry));
+    return m;
+}
+
+// The two keep bits of keep_carry (bit 0: low lane, bit 1: high lane).
+__device__ __forceinline__ uint32_t carry_bits(uint32_t carry) { return ((carry >> 15) & 1u) | ((carry >> 30) & 2u); }
+
 // Zeroes the dropped elements of a packed bf16 pair: the low 15 bits of both
 // lanes are added without crossing lanes, the carry out of each lane is the
 // majority of its top bits and the carry into them, and a byte permute spreads
@@ -381,6 +398,14 @@ __device__ __forceinline__ uint32_t apply_keep_fast(uint32_t data, uint32_t w, c
     uint32_t m;
     asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(carry));
     return data & m;
+}
+
+// AND mask of 32-bit word w (elements 2w, 2w + 1) of a 16-byte chunk whose
+// eight keep bits are the low byte of `bits` (bit e = element e).
+__device__ __forceinline__ uint32_t keep_mask_word(uint32_t bits, int w) {
+    const uint32_t lo = 0u - ((bits >> (2 * w)) & 1u);
+    const uint32_t hi = 0u - ((bits >> (2 * w + 1)) & 1u);
+    return (lo & 0x0000FFFFu) | (hi & 0xFFFF0000u);
 }
 
 // One Philox word covers two bf16 elements: the low 16-bit lane decides the

@@ -103,7 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
         tmem_alloc(tmem_slot, tmem_cols);
         tmem_relinquish();
     }
-    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapX);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.mapX);
+        if (p.use_bits) tma_prefetch_desc(&p.mapBits);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -127,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 const int rpad = p.rt.ad[d.a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                 uint8_t* st = smem + s * p.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], kXBytes + 256u * static_cast<uint32_t>(rpad));
+                mbar_arrive_expect_tx(&full[s], kXBytes + 256u * static_cast<uint32_t>(rpad) + (p.use_bits ? 2048u : 0u));
+                if (p.use_bits) tma_load_2d(st + p.off_bits, &p.mapBits, &full[s], d.fb * 16, d.tile * kTileM);
                 tma_load_2d(st, &p.mapX, &full[s], d.fb * 128, d.tile * kTileM);
                 tma_load_2d(st + 16384, &p.mapX, &full[s], d.fb * 128 + 64, d.tile * kTileM);
                 tma_load_2d(st + p.off_d, &p.mapD[d.a], &full[s], 0, d.tile * kTileM);
@@ -217,7 +221,24 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             const AdapterDev ad = p.rt.ad[d.a];
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            if (ad.T != 0u) {
+            if (ad.T != 0u && p.use_bits) {
+                // the forward's keep bits: byte cc of the row's 16 covers chunk cc (bit e = feature 8 cc + e)
+                const uint32_t sbase = smem_u32(smem + s * p.stage_bytes);
+                const uint32_t xrow = sbase + row * 128;
+                const uint4 kb4 = lds128(sbase + p.off_bits + row * 16);
+                const uint32_t kw[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
+#pragma unroll
+                for (int cc = 0; cc < kChunks; ++cc) {
+                    const uint32_t byte = kw[cc >> 2] >> (8 * (cc & 3));
+                    const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
+                    uint4 v = lds128(addr);
+                    v.x &= keep_mask_word(byte, 0);
+                    v.y &= keep_mask_word(byte, 1);
+                    v.z &= keep_mask_word(byte, 2);
+                    v.w &= keep_mask_word(byte, 3);
+                    sts128(addr, v);
+                }
+            } else if (ad.T != 0u) {
                 const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
                 const uint32_t t = static_cast<uint32_t>(static_cast<int64_t>(d.tile) * kTileM + row);
                 const uint32_t g0 = static_cast<uint32_t>(d.fb * 16);

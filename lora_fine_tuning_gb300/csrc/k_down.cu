@@ -34,6 +34,7 @@ constexpr int kGroupThreads = 128;                // a mask group: four warps, o
 constexpr int kGroups = kMaskWarps / 4;            // mask groups, taking stages in turn
 constexpr int kParts = kGroupThreads / 128;        // group threads per tile row
 constexpr int kChunks = 8 / kParts;                // 16-byte chunks (8 features) per thread and stage
+static_assert(kChunks == 8, "a thread owns a whole 64-feature row of its stage");
 static_assert(kGroupThreads == 128, "a group is four warps: one thread per tile row, one warp per TMEM lane quadrant");
 constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16; then 64 rows of A (rpad_max x 2 bytes each)
 
@@ -197,9 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             const uint32_t T = p.rt.ad[a].T;
             bool ok = mbar_wait(&full[s], ph, w, 4);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            if (T != 0u || p.mask_bits != nullptr) {
+            const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
+            uint32_t kbyte[kChunks];     // keep bits of each chunk (bit e = feature 8 (kb * 8 + i) + e)
+            if (T != 0u) {
                 const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
-                const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
                 if (static_cast<uint32_t>(t) != prow_t) {
                     prow_t = static_cast<uint32_t>(t);
                     prow = philox_row(prow_t, keys);
@@ -208,25 +210,35 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
 #pragma unroll
                 for (int i = 0; i < kChunks; ++i)
                     wv[i] = philox_10_row(prow, static_cast<uint32_t>(kb * 8 + i), keys);
-                if (T != 0u) {
-                    const KeepTest kt = keep_test(T);
+                const KeepTest kt = keep_test(T);
 #pragma unroll
-                    for (int i = 0; i < kChunks; ++i) {
-                        const uint32_t addr = xrow + ((i ^ (row & 7)) << 4);
-                        uint4 v = lds128(addr);
-                        v.x = apply_keep_fast(v.x, wv[i].x, kt);
-                        v.y = apply_keep_fast(v.y, wv[i].y, kt);
-                        v.z = apply_keep_fast(v.z, wv[i].z, kt);
-                        v.w = apply_keep_fast(v.w, wv[i].w, kt);
-                        sts128(addr, v);
-                    }
+                for (int i = 0; i < kChunks; ++i) {
+                    const uint32_t addr = xrow + ((i ^ (row & 7)) << 4);
+                    uint4 v = lds128(addr);
+                    const uint32_t c0 = keep_carry(wv[i].x, kt), c1 = keep_carry(wv[i].y, kt);
+                    const uint32_t c2 = keep_carry(wv[i].z, kt), c3 = keep_carry(wv[i].w, kt);
+                    v.x &= carry_mask(c0);
+                    v.y &= carry_mask(c1);
+                    v.z &= carry_mask(c2);
+                    v.w &= carry_mask(c3);
+                    sts128(addr, v);
+                    kbyte[i] = carry_bits(c0) | (carry_bits(c1) << 2) | (carry_bits(c2) << 4) | (carry_bits(c3) << 6);
                 }
-                if (p.mask_bits != nullptr && t < p.m) {
+            } else {
 #pragma unroll
-                    for (int i = 0; i < kChunks; ++i) {
-                        const int64_t g = static_cast<int64_t>(kb) * 8 + i;
-                        if (g * 8 < p.k) p.mask_bits[t * (p.k >> 3) + g] = static_cast<uint8_t>(keep_byte(wv[i], T));
-                    }
+                for (int i = 0; i < kChunks; ++i) kbyte[i] = 0xFFu;
+            }
+            if (p.mask_bits != nullptr && t < p.m) {
+                uint8_t* dst = p.mask_bits + t * (p.k >> 3) + static_cast<int64_t>(kb) * 8;
+                if ((p.k & 63) == 0) {
+                    // the row's eight bytes of this k-block in one aligned 8-byte store
+                    const uint32_t lo = kbyte[0] | (kbyte[1] << 8) | (kbyte[2] << 16) | (kbyte[3] << 24);
+                    const uint32_t hi = kbyte[4] | (kbyte[5] << 8) | (kbyte[6] << 16) | (kbyte[7] << 24);
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < kChunks; ++i)
+                        if ((static_cast<int64_t>(kb) * 8 + i) * 8 < p.k) dst[i] = static_cast<uint8_t>(kbyte[i]);
                 }
             }
             fence_proxy_async_smem();

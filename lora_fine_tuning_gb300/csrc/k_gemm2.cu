@@ -293,7 +293,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t keep[BN / 32];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c) keep[c] = 0u;
-            if (branch) {
+            if (branch && p.keep_bits != nullptr) {
+                // the forward's keep bits: 32 columns per little-endian word (bit e of byte g = column 8g + e)
+                if (row < p.M) {
+                    const uint32_t* kw = reinterpret_cast<const uint32_t*>(p.keep_bits + row * (p.N >> 3) + (n0 >> 3));
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c)
+                        if (n0 + c * 32 < p.N) keep[c] = __ldg(kw + c);
+                }
+            } else if (branch) {
                 const uint32_t T = p.rt.ad[a].T;
 #pragma unroll
                 for (int c = 0; c < BN / 32; ++c) {

@@ -85,6 +85,8 @@ struct GemmParams {
     int32_t nkb;                       // 64-deep K blocks of the main product
     uint32_t seed_lo, seed_hi;
     const float* col_scale;            // forward only, optional: output column j is multiplied by col_scale[j] (DoRA)
+    const uint8_t* keep_bits;          // backward only, optional: the forward's keep bits (m x N/8 bytes, N % 32 == 0),
+                                       // read instead of regenerating the mask
 };
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,
@@ -125,6 +127,9 @@ struct DaParams {
     uint32_t seed_lo, seed_hi;
     int32_t stages;
     uint32_t stage_bytes, off_d;
+    CUtensorMap mapBits;               // optional: the forward's keep bits {k/8, m} bytes, box {16, 128}, no swizzle
+    int32_t use_bits;                  // 1: the stage's keep bits come with X (at off_bits) instead of from Philox
+    uint32_t off_bits;
 };
 
 }  // namespace lora

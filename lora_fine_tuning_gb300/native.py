@@ -63,17 +63,17 @@ def lib() -> ctypes.CDLL:
         sig = {
             "lora_workspace_size": (sz, [i64, i64, i64, i32, i32]),
             "lora_fwd": (i32, [vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
-            "lora_bwd": (i32, [vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
+            "lora_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "multi_lora_fwd": (i32, [vp, vp, ctypes.POINTER(LoraAdapter), i32, ctypes.POINTER(LoraSegment), i32, u64,
                                      i64, i64, i64, vp, vp, vp, vp, sz, vp]),
             "multi_lora_bwd": (i32, [vp, vp, vp, ctypes.POINTER(LoraAdapter), i32, ctypes.POINTER(LoraSegment), i32,
-                                     u64, i64, i64, i64, vp, vp, vp, sz, vp]),
+                                     u64, i64, i64, i64, vp, vp, vp, vp, sz, vp]),
             "dora_workspace_size": (sz, [i64, i64, i64, i32]),
             "dora_weight_norm2": (i32, [vp, i64, i64, vp, vp]),
             "dora_fwd": (i32, [vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, vp, sz,
                                vp]),
-            "dora_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp,
-                               vp, vp, vp, sz, vp]),
+            "dora_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp,
+                               vp, vp, vp, vp, sz, vp]),
             "lora_fwd_static_scratch": (i32, [vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp]),
             "lora_tile_table": (i32, [ctypes.POINTER(LoraSegment), i32, i32, i64, ctypes.POINTER(ctypes.c_int32),
                                       i64]),

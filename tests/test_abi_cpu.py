@@ -119,8 +119,12 @@ def test_multi_validation_codes(lib):
     assert st == 8
     # the backward needs gradient buffers
     st = lib.multi_lora_bwd(256, 256, 256, ad, 2, native.segments_array([(0, 128, 0)]), 1, 0, 512, 64, 64, 256,
-                            256, 256, 1 << 30, None)
+                            None, 256, 256, 1 << 30, None)
     assert st == 1
+    # saved keep bits must be 16-byte aligned like every other buffer
+    st = lib.lora_bwd(256, 256, 256, 256, 256, 256, 264, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256, 256, 1 << 30,
+                      None)
+    assert st == 2
 
 
 @pytest.mark.parametrize("seed", range(12))
@@ -170,6 +174,6 @@ def test_dora_workspace_and_validation(lib):
     st = lib.dora_fwd(256, 256, 256, 256, 260, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256, None, 256,
                       1 << 30, None)
     assert st == 2
-    st = lib.dora_bwd(256, 256, 256, 256, 256, 256, 256, 256, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256, 256,
-                      None, 256, 256, 1 << 30, None)
+    st = lib.dora_bwd(256, 256, 256, 256, 256, 256, None, 256, 256, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256,
+                      256, None, 256, 256, 1 << 30, None)
     assert st == 1
