@@ -616,6 +616,17 @@ class DeviceProblem:
         return self.api.lora_device_status(self.ws, self.stream)
 
 
+WAIT_KERNELS = {1: "down_proj", 2: "gemm_fwd", 3: "gemm_bwd", 4: "ds_db", 5: "da", 6: "debug"}
+
+
+def check_status(prob, where: str) -> None:
+    """Raise if a kernel gave up a bounded wait (the workspace status word: kernel id << 8 | wait site)."""
+    code = prob.status()
+    if code != 0:
+        raise RuntimeError(f"a kernel reported a bounded-wait timeout {where}: status 0x{code:x} "
+                           f"({WAIT_KERNELS.get(code >> 8, 'unknown kernel')}, wait site {code & 0xFF})")
+
+
 def timed_loop(fn, steps, stream, flush=None):
     """Device milliseconds of `steps` calls of fn, on `stream`.  With `flush`, L2 is overwritten
     before every call and only the calls themselves are timed (per-call event pairs)."""
@@ -709,8 +720,7 @@ def e2e_leg(prob_a, prob_b, wl, dev, stream, steps, barrier, max_over_ranks, ws_
     barrier()
     ms_serial = max_over_ranks(timed_loop(serial, steps, stream))
     for p in sets:
-        if p.status() != 0:
-            raise RuntimeError("a kernel reported a bounded-wait timeout in the end-to-end leg")
+        check_status(p, "in the end-to-end leg")
     h2d = sum(h.numel() * h.element_size() for h, _ in sets[0].inputs.values())
     d2h = sum(h.numel() * h.element_size() for h in hosts[0])
     return {"value": job_throughput(wl.tokens, steps, ws_n, ms), "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -751,8 +761,7 @@ def run_native(args):
     for _ in range(args.warmup):
         prob.step()
     torch.cuda.synchronize(dev)
-    if prob.status() != 0:
-        raise RuntimeError("a kernel reported a bounded-wait timeout during warm-up")
+    check_status(prob, "during warm-up")
 
     # --- timed region (device, inputs resident in HBM, nothing between the library's launches) ---
     with ClockSampler(local) as clocks:
@@ -764,8 +773,7 @@ def run_native(args):
         barrier()
     elapsed_ms = max_over_ranks(elapsed_ms)
     clk = clocks.summary()
-    if prob.status() != 0:
-        raise RuntimeError("a kernel reported a bounded-wait timeout in the timed region")
+    check_status(prob, "in the timed region")
 
     # --- per-kernel breakdown: a second timed region of the same steps with an event pair around every
     # launch (on the launch stream); the events also keep consecutive kernels from overlapping ---
@@ -773,8 +781,7 @@ def run_native(args):
     native.timing_begin()
     instrumented_ms = timed_loop(prob.step, args.steps, stream, flush)
     kernel_times = native.timing_end()
-    if prob.status() != 0:
-        raise RuntimeError("a kernel reported a bounded-wait timeout in the instrumented region")
+    check_status(prob, "in the instrumented region")
 
     ms_per_step = elapsed_ms / args.steps
     value = job_throughput(wl.tokens, args.steps, ws_n, elapsed_ms)

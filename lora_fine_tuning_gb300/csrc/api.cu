@@ -388,7 +388,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         p.seed_lo = seed_lo;
         p.seed_hi = seed_hi;
         p.stage_bytes = 16384u + 128u * static_cast<uint32_t>(c.rt.rpad_max);
-        p.stages = static_cast<int32_t>(std::min<size_t>(12, kStageBudget / p.stage_bytes));
+        p.stages = mask_ring_stages(p.stage_bytes, 12);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
         LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));
@@ -549,7 +549,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             p.off_bits = p.stage_bytes;
             p.stage_bytes += 2048;
         }
-        p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
+        p.stages = mask_ring_stages(p.stage_bytes, 8);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side); }));
         LORA_CUDA(cudaEventRecord(ev_join, side));
@@ -597,7 +597,7 @@ lora_status run_dora_norm(const Call& c, const DoraFwd& d, const uint16_t* W, co
     for (int a = 1; a <= kMaxAdapters; ++a) pu.unit_begin[a] = pu.units;
     pu.off_d = 32768;
     pu.stage_bytes = pu.off_d + 256 * static_cast<uint32_t>(rp);
-    pu.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / pu.stage_bytes));
+    pu.stages = mask_ring_stages(pu.stage_bytes, 8);
     const int grid = static_cast<int>(std::min<int64_t>(pu.units, c.sms));
     LORA_CUDA(timed(kDoraU, c.stream, [&] { return launch_da(pu, grid, c.stream); }));
     LORA_CUDA(timed(kDoraNorm, c.stream, [&] {

@@ -27,11 +27,11 @@ namespace lora {
 
 namespace {
 
-constexpr int kMaskWarps = 8;                      // warps 2..9 mask, and run the epilogue
+constexpr int kMaskWarps = 4 * kMaskGroups;        // warps 2.. mask, and run the epilogue
 constexpr int kMaskThreads = 32 * kMaskWarps;
 constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
 constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
-constexpr int kGroups = kMaskWarps / 4;            // mask groups, taking stages in turn
+constexpr int kGroups = kMaskGroups;               // mask groups, taking stages in turn (S % kGroups == 0)
 constexpr int kParts = kGroupThreads / 128;        // group threads per tile row
 constexpr int kChunks = 8 / kParts;                // 16-byte chunks (8 features) per thread and stage
 static_assert(kChunks == 8, "a thread owns a whole 64-feature row of its stage");
@@ -42,6 +42,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
+    if (S < kGroups || S % kGroups != 0) {
+        // every stage must belong to one mask group (the host rounds the ring to a multiple of kGroups)
+        if (threadIdx.x == 0 && p.ctl.status) atomicCAS(p.ctl.status, 0, (kKDown << 8) | 0xFF);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
     uint64_t* full = bars;
     uint64_t* masked = bars + S;
