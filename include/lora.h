@@ -264,7 +264,9 @@ const char* lora_status_string(lora_status s);
  * fills, for each kind i < n_kinds (see lora_kernel_name), the summed device
  * time in ms and the number of launches.  Kinds: 0 down-projection,
  * 1 finalize S, 2 forward GEMM, 3 dS/dB, 4 finalize dS/dB, 5 backward GEMM,
- * 6 dA, 7 finalize dA, 8 memset (gradients of adapters that own no rows).
+ * 6 dA, 7 finalize dA, 8 memset (gradients of adapters that own no rows),
+ * 9-12 DoRA (U, norm, dZ, dmag).  Kind 6 runs on the library's side stream
+ * beside the backward GEMM; its event pair spans from the fork to its end.
  * Host-side cost: two event records per launch. */
 enum { LORA_KERNEL_KINDS = 13 };
 lora_status lora_timing_begin(void);

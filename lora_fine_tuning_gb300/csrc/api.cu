@@ -471,7 +471,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
-        LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, c.sms, c.stream); }));
+        LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs | kPartDb, c.sms, c.stream); }));
     }
 
     // dA only needs dSq (written above) and X, not dX: it is forked onto the side stream, launched after
@@ -551,10 +551,12 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         }
         p.stages = mask_ring_stages(p.stage_bytes, 8);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
-        LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side); }));
+        // plain launches on both sides of the event waits: a programmatic launch could start before the
+        // other stream's work it waits for is done
+        LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side, false); }));
         LORA_CUDA(cudaEventRecord(ev_join, side));
         LORA_CUDA(cudaStreamWaitEvent(c.stream, ev_join, 0));
-        LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(p, c.sms, c.stream); }));
+        LORA_CUDA(timed(kFinalizeDa, c.stream, [&] { return launch_finalize_da(p, c.sms, c.stream, false); }));
     }
     return LORA_OK;
 }

@@ -360,13 +360,13 @@ cudaError_t da_configure() {
     return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
-cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream) {
-    return launch_pdl(da_kernel, dim3(grid), dim3(kThreads), da_smem_bytes(p), stream, p);
+cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream, bool pdl) {
+    return launch_k(pdl, da_kernel, dim3(grid), dim3(kThreads), da_smem_bytes(p), stream, p);
 }
 
-cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream) {
-    return launch_pdl(finalize_da_kernel, dim3(2 * sms), dim3(256), 0, stream, p.acc_base, p.k, p.dsq, p.m, p.ld,
-                      p.rt, p.dA);
+cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream, bool pdl) {
+    return launch_k(pdl, finalize_da_kernel, dim3(2 * sms), dim3(256), 0, stream, p.acc_base, p.k, p.dsq, p.m, p.ld,
+                    p.rt, p.dA);
 }
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream) {

@@ -243,46 +243,49 @@ __global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant
 }
 
 // dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0, on
-// rows of active tiles; dB_a[c, j] = bf16(dB^T_acc_a[j, c]).  Every
-// accumulator read is cleared.
+// rows of active tiles (parts & kPartDs); dB_a[c, j] = bf16(dB^T_acc_a[j, c])
+// (parts & kPartDb).  Every accumulator read is cleared.
 __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
                                      float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
-                                     const __grid_constant__ AdapterPtrs dbp) {
+                                     const __grid_constant__ AdapterPtrs dbp, int32_t parts) {
     pdl_wait();
     pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    // dS: one thread per 8 columns of a row (m * ld / 8 < 2^31: 32-bit index arithmetic)
-    const uint32_t g8 = static_cast<uint32_t>(ld / 8);
-    const uint32_t total_s = static_cast<uint32_t>(m) * g8;
-    for (uint32_t i = static_cast<uint32_t>(tid); i < total_s; i += static_cast<uint32_t>(stride)) {
-        const uint32_t t = i / g8;
-        const int c0 = static_cast<int>(i - t * g8) * 8;
-        const int a = rt.tile_adapter[t >> 7];
-        if (a < 0) continue;
-        const int valid = rt.ad[a].rank;
-        float v[8];
-        if (c0 < valid) {
-            float* src = dS_acc + static_cast<int64_t>(t) * ld + c0;
-            const float4 x = ld_l2_f4(src);
-            const float4 y = ld_l2_f4(src + 4);
-            v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
-            st_zero_f4(src);
-            st_zero_f4(src + 4);
-        }
+    if (parts & kPartDs) {
+        // dS: one thread per 8 columns of a row (m * ld / 8 < 2^31: 32-bit index arithmetic)
+        const uint32_t g8 = static_cast<uint32_t>(ld / 8);
+        const uint32_t total_s = static_cast<uint32_t>(m) * g8;
+        for (uint32_t i = static_cast<uint32_t>(tid); i < total_s; i += static_cast<uint32_t>(stride)) {
+            const uint32_t t = i / g8;
+            const int c0 = static_cast<int>(i - t * g8) * 8;
+            const int a = rt.tile_adapter[t >> 7];
+            if (a < 0) continue;
+            const int valid = rt.ad[a].rank;
+            float v[8];
+            if (c0 < valid) {
+                float* src = dS_acc + static_cast<int64_t>(t) * ld + c0;
+                const float4 x = ld_l2_f4(src);
+                const float4 y = ld_l2_f4(src + 4);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w; v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+                st_zero_f4(src);
+                st_zero_f4(src + 4);
+            }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * rt.ad[a].scale : 0.f;
-        uint4 pk;
-        pk.x = pack_bf16x2(v[0], v[1]);
-        pk.y = pack_bf16x2(v[2], v[3]);
-        pk.z = pack_bf16x2(v[4], v[5]);
-        pk.w = pack_bf16x2(v[6], v[7]);
-        stg128(dSq + static_cast<int64_t>(t) * ld + c0, pk);
+            for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * rt.ad[a].scale : 0.f;
+            uint4 pk;
+            pk.x = pack_bf16x2(v[0], v[1]);
+            pk.y = pack_bf16x2(v[2], v[3]);
+            pk.z = pack_bf16x2(v[4], v[5]);
+            pk.w = pack_bf16x2(v[6], v[7]);
+            stg128(dSq + static_cast<int64_t>(t) * ld + c0, pk);
+        }
     }
+    if (!(parts & kPartDb)) return;
     // dB_a = (dB^T_acc_a)^T.  Lane i of a warp owns accumulator row j = 32 w + i (rpad floats, read 16 at a
     // time, contiguous across the warp) and writes those values down column j of dB, so every store of the
-    // warp is 32 consecutive bf16 of one row of dB.  No shared memory, so under programmatic launch these
-    // CTAs can sit beside the CTAs of the GEMM that follows.
+    // warp is 32 consecutive bf16 of one row of dB.  No shared memory and few registers, so these CTAs fit
+    // beside the dX GEMM's CTAs on the same SMs.
     const int lane = threadIdx.x & 31;
     const int64_t n_warps = stride / 32, gw = tid / 32;
     const int64_t per_adapter = (n + 31) / 32;   // warp tasks of one adapter; tasks of all adapters share the warps
@@ -333,9 +336,10 @@ cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
     return launch_pdl(dsdb_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
 }
 
-cudaError_t launch_finalize_bwd1(const DsDbParams& p, int sms, cudaStream_t stream) {
-    return launch_pdl(finalize_bwd1_kernel, dim3(2 * sms), dim3(256), 0, stream, p.dS_acc, p.dSq, p.m, p.ld,
-                      p.acc_base, p.n, p.rt, p.dB);
+cudaError_t launch_finalize_bwd1(const DsDbParams& p, int parts, int sms, cudaStream_t stream, bool pdl) {
+    if (parts < kPartDs || parts > (kPartDs | kPartDb)) return cudaErrorInvalidValue;
+    return launch_k(pdl, finalize_bwd1_kernel, dim3(2 * sms), dim3(256), 0, stream, p.dS_acc, p.dSq, p.m, p.ld,
+                    p.acc_base, p.n, p.rt, p.dB, static_cast<int32_t>(parts));
 }
 
 }  // namespace lora

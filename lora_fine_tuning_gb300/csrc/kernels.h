@@ -13,9 +13,14 @@ namespace lora {
 // Launches a kernel on `stream` with programmatic stream serialization: it may
 // start while the previous kernel on the stream finishes, and waits for it with
 // griddepcontrol.wait before touching global memory.
+//
+// `pdl` false gives a plain launch.  A kernel whose stream waits on another
+// stream's event just before it is launched plainly: with the attribute it
+// could start once the previous kernel of its own stream triggers, before the
+// other stream's work is done.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
+cudaError_t launch_k(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -25,8 +30,14 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    return launch_k(true, kernel, grid, block, smem, stream, std::forward<Args>(args)...);
 }
 
 // Dynamic shared memory a kernel may request; leaves room for its few bytes
@@ -59,12 +70,14 @@ cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStr
 size_t dsdb_smem_bytes(const DsDbParams& p);
 cudaError_t dsdb_configure();
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_finalize_bwd1(const DsDbParams& p, int sms, cudaStream_t stream);
+// finalize_bwd1 parts: dSq from dS (the dX GEMM and dA need it) and dB from dB^T (an output only).
+constexpr int kPartDs = 1, kPartDb = 2;
+cudaError_t launch_finalize_bwd1(const DsDbParams& p, int parts, int sms, cudaStream_t stream, bool pdl = true);
 
 size_t da_smem_bytes(const DaParams& p);
 cudaError_t da_configure();
-cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream);
+cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream, bool pdl = true);
+cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream, bool pdl = true);
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream);
 

@@ -58,6 +58,7 @@ def test_tiny_workload():
     (256, 4096, 320, 16, 2.0, 0.1, 2**33 + 5),  # many k blocks: a tile split over CTAs; seed above 2^32
     (640, 192, 2048, 32, 4.0, 0.5, 15),      # many n blocks in the dS/dB pass
     (1, 64, 64, 16, 1.0, 0.1, 16),           # one row
+    (2048, 8192, 64, 16, 2.0, 0.1, 17),      # short dX GEMM (K = 64), long dA pass beside it: the join must wait
 ])
 def test_single_shapes(m, k, n, r, alpha, p, seed):
     raw, out = run_single(m, k, n, r, alpha, p, seed)
