@@ -1,8 +1,10 @@
 """GPU parity at the benchmark sizes, in the launch configuration the benchmark times.
 
-The oracle computes, in fp64 on the host: the full keep mask, S, dS-derived
-dA and dB (all O(m r (k + n))), and Y / dX on a sample of rows (256 random rows
-plus two whole 128-row tiles), which it computes one row at a time.
+As in bench.py, the forward writes the keep bits and the backward reads them,
+and one workspace serves both calls (its status word is checked after).  The
+oracle computes, in fp64 on the host: the full keep mask, S, dS-derived dA and
+dB (all O(m r (k + n))), and Y / dX on a sample of rows (256 random rows plus
+two whole 128-row tiles), which it computes one row at a time.
 """
 import numpy as np
 import pytest
@@ -34,10 +36,11 @@ def test_single_adapter_full_size(name):
     m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
     raw = synth.layer_inputs(seed, m, k, n, r)
     X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
-    Y, S, mask = api.lora_fwd(X, W, A, B, alpha, p, seed, want_mask=True)
-    dX, dA, dB = api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed)
+    ws = api.workspace(m, k, n, r)
+    Y, S, mask = api.lora_fwd(X, W, A, B, alpha, p, seed, want_mask=True, ws=ws)
+    dX, dA, dB = api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed, ws=ws, mask_bits=mask)
     torch.cuda.synchronize()
-    assert api.lora_device_status(api.workspace(m, k, n, r)) == 0
+    assert api.lora_device_status(ws) == 0
 
     Xo = O.bf16_to_f64(raw["X"])
     Ao, Bo = O.bf16_to_f64(raw["A"]), O.bf16_to_f64(raw["B"])
@@ -69,9 +72,11 @@ def test_multi_adapter_full_size():
     raw = synth.multi_inputs(seed, k, n, specs, batch)
     X, W, dY = (to_dev(raw[x]) for x in ("X", "W", "dY"))
     adapters = [api.Adapter(A=to_dev(A), B=to_dev(B), alpha=s.alpha, p=s.p) for (A, B), s in zip(raw["adapters"], specs)]
-    Y, S, mask = api.multi_lora_fwd(X, W, adapters, batch.segments, seed, want_mask=True)
-    dX = api.multi_lora_bwd(dY, X, W, adapters, batch.segments, seed, S)
+    ws = api.workspace(batch.m, k, n, max(s.rank for s in specs), len(specs))
+    Y, S, mask = api.multi_lora_fwd(X, W, adapters, batch.segments, seed, want_mask=True, ws=ws)
+    dX = api.multi_lora_bwd(dY, X, W, adapters, batch.segments, seed, S, ws=ws, mask_bits=mask)
     torch.cuda.synchronize()
+    assert api.lora_device_status(ws) == 0
 
     m = batch.m
     Xo, dYo = O.bf16_to_f64(raw["X"]), O.bf16_to_f64(raw["dY"])
@@ -108,3 +113,49 @@ def test_multi_adapter_full_size():
                                                   ad["p"], seed, rows[pick])
             dXr[pick] += dXb
     assert_close("dX[rows]", host_f64(dX[torch.from_numpy(rows).cuda()]), dXr)
+
+
+def test_dora_full_size():
+    """The Llama-3.1-8B up-proj as DoRA, as bench.py's DoRA workload runs it."""
+    cfg = synth.WORKLOADS["llama8b_up"]
+    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
+    raw = synth.layer_inputs(seed, m, k, n, r)
+    X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
+    Wo, Ao, Bo = (O.bf16_to_f64(raw[x]) for x in ("W", "A", "B"))
+    rng = np.random.default_rng(seed + 100)
+    mag_h = (np.sqrt((Wo ** 2).sum(0)) * rng.uniform(0.8, 1.2, n)).astype(np.float32)
+    mag = torch.from_numpy(mag_h).cuda()
+    ws = api.dora_workspace(m, k, n, r)
+    wn2 = api.dora_weight_norm2(W)
+    Y, S, g, mask = api.dora_fwd(X, W, A, B, mag, wn2, alpha, p, seed, want_mask=True, ws=ws)
+    dX, dA, dB, dmag = api.dora_bwd(dY, X, W, A, B, S, Y, mag, g, alpha, p, seed, ws=ws, mask_bits=mask)
+    torch.cuda.synchronize()
+    assert api.lora_device_status(ws) == 0
+
+    norms = O.dora_column_norms(Wo, Ao, Bo, alpha)
+    gr = mag_h.astype(np.float64) / norms
+    assert_close("g", g.double().cpu().numpy(), gr, 1e-4)
+    Xo, dYo = O.bf16_to_f64(raw["X"]), O.bf16_to_f64(raw["dY"])
+    T, q = O.dropout_threshold(p), O.dropout_scale(p)
+    D = O.keep_mask(seed, np.arange(m), k, T)
+    np.testing.assert_array_equal(mask.cpu().numpy(), O.pack_mask_bits(D))
+    Xhat = Xo * D * q
+    del D
+    Sr = Xhat @ Ao
+    assert_close("S_saved", host_f64(S), alpha * Sr)
+    dZ = dYo * gr                                   # the norm is held constant in the backward
+    dSr = alpha * (dZ @ Bo.T)
+    assert_close("dB", host_f64(dB), alpha * (Sr.T @ dZ))
+    assert_close("dA", host_f64(dA), Xhat.T @ dSr)
+    del Xhat, dZ
+
+    rows = sample_rows(m, seed)
+    Yr, _, _, _, _ = O.dora_forward(Xo[rows], Wo, Ao, Bo, mag_h, alpha, p, seed, rows=rows)
+    assert_close("Y[rows]", host_f64(Y[torch.from_numpy(rows).cuda()]), Yr)
+    dXr, _, _, _ = O.dora_backward(dYo[rows], Xo[rows], Wo, Ao, Bo, mag_h, alpha, p, seed, rows=rows)
+    assert_close("dX[rows]", host_f64(dX[torch.from_numpy(rows).cuda()]), dXr)
+    # dmag on a sample of columns: sum over all m rows of dY Z / norm, Z from the definition
+    cols = np.sort(rng.choice(n, size=64, replace=False))
+    Zc = Xo @ Wo[:, cols] + alpha * (Sr @ Bo[:, cols])
+    dmag_r = (dYo[:, cols] * Zc).sum(0) / norms[cols]
+    assert_close("dmag[cols]", dmag.double().cpu().numpy()[cols], dmag_r)
