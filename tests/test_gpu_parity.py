@@ -235,16 +235,17 @@ def test_stuck_wait_reports_timeout_and_context_survives():
     check_single_full(raw, out, 1.0, 0.1, 5)
 
 
-def test_workspace_is_left_zeroed():
-    """Each call leaves the workspace all zeros, so calls of any shape can share it."""
-    m, k, n, r = 640, 1032, 392, 24
+@pytest.mark.parametrize("m,k,n,r,saved_bits", [(640, 1032, 392, 24, False), (640, 1024, 392, 24, True)])
+def test_workspace_is_left_zeroed(m, k, n, r, saved_bits):
+    """Each call leaves the workspace all zeros, so calls of any shape can share it (also when the backward
+    reads the forward's keep bits: k % 128 == 0 takes the bits path in both backward kernels)."""
     raw = synth.layer_inputs(51, m, k, n, r)
     X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
     ws = torch.zeros(api.lora_workspace_size(m, k, n, r), dtype=torch.uint8, device="cuda")
-    Y, S, _ = api.lora_fwd(X, W, A, B, 1.0, 0.2, 51, ws=ws)
+    Y, S, bits = api.lora_fwd(X, W, A, B, 1.0, 0.2, 51, ws=ws, want_mask=saved_bits)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
-    api.lora_bwd(dY, X, W, A, B, S, 1.0, 0.2, 51, ws=ws)
+    api.lora_bwd(dY, X, W, A, B, S, 1.0, 0.2, 51, ws=ws, mask_bits=bits)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
 
