@@ -500,7 +500,7 @@ def cpu_baseline_leg(wl: Workload, seconds: float):
 class DeviceProblem:
     """The workload's tensors on the GPU plus pinned host copies, and one step through the C ABI."""
 
-    def __init__(self, wl: Workload, dev, stream):
+    def __init__(self, wl: Workload, dev, stream, saved_mask: bool = False):
         import torch
 
         from lora_fine_tuning_gb300 import api
@@ -531,7 +531,9 @@ class DeviceProblem:
                      W=weight(q.W), Y=torch.empty((m, q.n), dtype=bf, device=dev),
                      dX=torch.empty((m, q.k), dtype=bf, device=dev),
                      S=torch.empty((m, q.r_max), dtype=bf, device=dev),
-                     M=torch.empty((m, q.k // 8), dtype=torch.uint8, device=dev),   # keep bits, fwd -> bwd
+                     # keep bits written by the forward and read by the backward (saved-mask mode only;
+                     # otherwise the backward regenerates the mask from the seed)
+                     M=torch.empty((m, q.k // 8), dtype=torch.uint8, device=dev) if saved_mask else None,
                      adapters=[api.Adapter(A=weight(A), B=weight(B), alpha=a, p=p,
                                            dA=torch.empty((q.k, r), dtype=bf, device=dev),
                                            dB=torch.empty((r, q.n), dtype=bf, device=dev))
@@ -743,7 +745,7 @@ def run_native(args):
     dev = torch.device("cuda", local)
     wl = Workload(args.workload, args.m, args.r, packer=native.pack_microbatches)
     stream = torch.cuda.current_stream(dev)
-    prob = DeviceProblem(wl, dev, stream)
+    prob = DeviceProblem(wl, dev, stream, args.saved_mask)
 
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = None
@@ -789,7 +791,7 @@ def run_native(args):
     # --- end to end through the public API with host buffers ---
     e2e = None
     if not args.no_e2e:
-        e2e = e2e_leg(prob, DeviceProblem(wl, dev, stream), wl, dev, stream, max(4, min(args.steps, 20)),
+        e2e = e2e_leg(prob, DeviceProblem(wl, dev, stream, args.saved_mask), wl, dev, stream, max(4, min(args.steps, 20)),
                       barrier, max_over_ranks, ws_n)
 
     # --- frozen-layer reference points (overhead of the LoRA branch) ---
@@ -855,7 +857,8 @@ def run_native(args):
     config = {"workload": wl.describe(), "m": wl.m, "k": [q.k for q in wl.parts], "n": [q.n for q in wl.parts],
               "r": [[r for r, _, _ in q.specs] for q in wl.parts], "tokens_per_step": wl.tokens,
               "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU", "l2": l2_note,
-              "saved_for_backward": "S_saved and the keep bits (m x k/8 bytes) written by the forward"}
+              "saved_for_backward": ("S_saved and the keep bits (m x k/8 bytes) written by the forward"
+                                     if args.saved_mask else "S_saved; the backward regenerates the keep mask from the seed")}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, Llama-shaped)", "config": config,
@@ -884,6 +887,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-frozen", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--saved-mask", action="store_true",
+                    help="the forward writes the keep bits and the backward reads them (default: regenerated)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

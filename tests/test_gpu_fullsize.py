@@ -1,7 +1,9 @@
 """GPU parity at the benchmark sizes, in the launch configuration the benchmark times.
 
-As in bench.py, the forward writes the keep bits and the backward reads them,
-and one workspace serves both calls (its status word is checked after).  The
+As in bench.py, one workspace serves both calls (its status word is checked
+after); the backward regenerates the keep mask from the seed, as bench.py does
+by default, and the 8B case also runs the saved-mask mode (bench.py
+--saved-mask: the forward writes the keep bits and the backward reads them).  The
 oracle computes, in fp64 on the host: the full keep mask, S, dS-derived dA and
 dB (all O(m r (k + n))), and Y / dX on a sample of rows (256 random rows plus
 two whole 128-row tiles), which it computes one row at a time.
@@ -30,15 +32,15 @@ def sample_rows(m, seed):
     return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("name", ["llama8b_up", "llama70b_o_r64"])
-def test_single_adapter_full_size(name):
+@pytest.mark.parametrize("name,saved", [("llama8b_up", False), ("llama8b_up", True), ("llama70b_o_r64", False)])
+def test_single_adapter_full_size(name, saved):
     cfg = synth.WORKLOADS[name]
     m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
     raw = synth.layer_inputs(seed, m, k, n, r)
     X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
     ws = api.workspace(m, k, n, r)
     Y, S, mask = api.lora_fwd(X, W, A, B, alpha, p, seed, want_mask=True, ws=ws)
-    dX, dA, dB = api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed, ws=ws, mask_bits=mask)
+    dX, dA, dB = api.lora_bwd(dY, X, W, A, B, S, alpha, p, seed, ws=ws, mask_bits=mask if saved else None)
     torch.cuda.synchronize()
     assert api.lora_device_status(ws) == 0
 
@@ -74,7 +76,7 @@ def test_multi_adapter_full_size():
     adapters = [api.Adapter(A=to_dev(A), B=to_dev(B), alpha=s.alpha, p=s.p) for (A, B), s in zip(raw["adapters"], specs)]
     ws = api.workspace(batch.m, k, n, max(s.rank for s in specs), len(specs))
     Y, S, mask = api.multi_lora_fwd(X, W, adapters, batch.segments, seed, want_mask=True, ws=ws)
-    dX = api.multi_lora_bwd(dY, X, W, adapters, batch.segments, seed, S, ws=ws, mask_bits=mask)
+    dX = api.multi_lora_bwd(dY, X, W, adapters, batch.segments, seed, S, ws=ws)
     torch.cuda.synchronize()
     assert api.lora_device_status(ws) == 0
 
@@ -128,7 +130,7 @@ def test_dora_full_size():
     ws = api.dora_workspace(m, k, n, r)
     wn2 = api.dora_weight_norm2(W)
     Y, S, g, mask = api.dora_fwd(X, W, A, B, mag, wn2, alpha, p, seed, want_mask=True, ws=ws)
-    dX, dA, dB, dmag = api.dora_bwd(dY, X, W, A, B, S, Y, mag, g, alpha, p, seed, ws=ws, mask_bits=mask)
+    dX, dA, dB, dmag = api.dora_bwd(dY, X, W, A, B, S, Y, mag, g, alpha, p, seed, ws=ws)
     torch.cuda.synchronize()
     assert api.lora_device_status(ws) == 0
 
