@@ -37,8 +37,8 @@
  *    with lora_device_status().
  *  - Validation happens before any launch; a failing call enqueues nothing
  *    and returns a status.  Nothing is thrown across this interface.
- *  - k and n must be multiples of 8, ranks multiples of 8 in [8, 128], every
- *    pointer 16-byte aligned, 0 <= p < 1, m <= 262144 rows.
+ *  - k and n must be multiples of 8 in [8, 2^24], ranks multiples of 8 in
+ *    [8, 128], every pointer 16-byte aligned, 0 <= p < 1, m <= 262144 rows.
  *  - Gradients dA, dB are overwritten, not accumulated.
  *  - `workspace` is device memory of at least lora_workspace_size() bytes,
  *    256-byte aligned, filled with zeros before its first use (cudaMemset).
@@ -62,7 +62,7 @@ typedef enum {
     LORA_OK = 0,
     LORA_EINVAL = 1,          /* missing pointer, p outside [0,1), rank outside [8,128], ... */
     LORA_EALIGN = 2,          /* a pointer is not 16-byte aligned (workspace: 256) */
-    LORA_ESHAPE = 3,          /* k or n not a multiple of 8, m too large, empty k or n */
+    LORA_ESHAPE = 3,          /* k or n not a multiple of 8 or above 2^24, m too large, empty k or n */
     LORA_EARCH = 4,           /* the current device is not an sm_103 GPU */
     LORA_ECUDA = 5,           /* a CUDA runtime or driver call failed */
     LORA_EWORKSPACE = 6,      /* workspace missing, misaligned or too small */
@@ -70,7 +70,8 @@ typedef enum {
     LORA_ETABLE = 8           /* segment table invalid: overlap, misalignment, bad adapter id */
 } lora_status;
 
-enum { LORA_TILE_ROWS = 128, LORA_MAX_RANK = 128, LORA_MAX_ADAPTERS = 16, LORA_MAX_ROWS = 262144 };
+enum { LORA_TILE_ROWS = 128, LORA_MAX_RANK = 128, LORA_MAX_ADAPTERS = 16, LORA_MAX_ROWS = 262144,
+       LORA_MAX_FEATURES = 16777216 /* k and n */ };
 
 /* One adapter of the multi-adapter form.  A_i is k x rank, B_i is rank x n;
  * dA_i / dB_i (same shapes) are written by multi_lora_bwd and may be NULL

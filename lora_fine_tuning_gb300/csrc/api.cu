@@ -191,7 +191,8 @@ lora_status check_dims(int64_t m, int64_t k, int64_t n) {
     if (m < 0 || k <= 0 || n <= 0) return LORA_ESHAPE;
     if (k % 8 || n % 8) return LORA_ESHAPE;
     if (m > LORA_MAX_ROWS) return LORA_ESHAPE;
-    if (k > (1LL << 30) || n > (1LL << 30)) return LORA_ESHAPE;
+    // at most 2^24 features: every per-feature count (k * rank / 8, n blocks, units) then fits 32 bits
+    if (k > LORA_MAX_FEATURES || n > LORA_MAX_FEATURES) return LORA_ESHAPE;
     return LORA_OK;
 }
 
@@ -842,7 +843,7 @@ size_t dora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r) {
 
 lora_status dora_weight_norm2(const lora_bf16* W, int64_t k, int64_t n, float* w_norm2, void* stream) {
     if (!W || !w_norm2) return LORA_EINVAL;
-    if (k <= 0 || n <= 0 || n % 8) return LORA_ESHAPE;
+    if (k <= 0 || n <= 0 || n % 8 || k > LORA_MAX_FEATURES || n > LORA_MAX_FEATURES) return LORA_ESHAPE;
     if (!aligned16(W) || !aligned16(w_norm2)) return LORA_EALIGN;
     int sms = 0;
     lora_status st;

@@ -92,6 +92,8 @@ def test_validation_codes_without_launching(lib):
     assert _fwd_status(lib, k=60) == 3          # k not a multiple of 8
     assert _fwd_status(lib, n=0) == 3           # empty n
     assert _fwd_status(lib, m=300000) == 3      # too many rows
+    assert _fwd_status(lib, k=(1 << 24) + 8) == 3   # more features than the 32-bit counts allow
+    assert _fwd_status(lib, n=(1 << 24) + 8) == 3
     assert _fwd_status(lib, r=12) == 1          # rank not a multiple of 8
     assert _fwd_status(lib, r=136) == 1         # rank above 128
     assert _fwd_status(lib, p=1.0) == 1         # p outside [0, 1)

@@ -32,7 +32,8 @@ def sample_rows(m, seed):
     return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("name,saved", [("llama8b_up", False), ("llama8b_up", True), ("llama70b_o_r64", False)])
+@pytest.mark.parametrize("name,saved", [("llama8b_up", False), ("llama8b_up", True), ("llama70b_o_r64", False),
+                                        ("llama70b_up_r64", False)])   # the largest layer of the benchmark set
 def test_single_adapter_full_size(name, saved):
     cfg = synth.WORKLOADS[name]
     m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))

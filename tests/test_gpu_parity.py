@@ -178,6 +178,18 @@ def test_multi_adapter_packed_batch(k, n, rows, gap, unused):
     check_multi(k, n, segments, raw, MULTI_SPECS, seed, adapters, Y, S, mask, dX)
 
 
+def test_maximum_rows_and_adapters():
+    """The row limit (262144 rows = 2048 tiles) with every adapter slot in use, ranks 8 to 128 (the limit), and
+    ragged k and n: masks bit-exact and every output against the oracle."""
+    specs = [synth.AdapterSpec(8 * (i + 1), (1.0, 2.0, 0.5, 4.0)[i % 4], (0.0, 0.1, 0.25, 0.5)[i % 4])
+             for i in range(16)]
+    k, n, m, seed = 136, 200, 262144, 71
+    batch, segments, raw = multi_case(k, n, m, specs, seed)
+    assert batch.m == m and len({s[2] for s in segments}) == 16
+    adapters, Y, S, mask, dX = run_multi(k, n, segments, raw, specs, seed)
+    check_multi(k, n, segments, raw, specs, seed, adapters, Y, S, mask, dX)
+
+
 def test_routing_table_matches_oracle():
     batch = synth.packed_batch(3, 16384, 4)
     from lora_fine_tuning_gb300 import native
