@@ -469,8 +469,14 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.off_b = 32768;
         p.off_s = p.off_b + 2 * 128 * rpm;
         p.stage_bytes = p.off_s + 256 * rpm;
-        p.stages = static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
-        const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        // Every small MMA of this pass costs its CTA's one issuing thread about 100 cycles, whatever its N.
+        // So when two stages fit in half the shared memory (padded rank <= 32), two CTAs share each SM,
+        // each with a two-stage ring and half the units per issuer.  Larger ranks keep one CTA per SM
+        // with the full ring.
+        const bool two_per_sm = 2u * p.stage_bytes <= kStageBudget / 2 - 2048;
+        p.stages = two_per_sm ? 2 : static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
+        const int64_t ctas = static_cast<int64_t>(two_per_sm ? 2 : 1) * c.sms;
+        const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
         LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
         LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs | kPartDb, c.sms, c.stream); }));
     }

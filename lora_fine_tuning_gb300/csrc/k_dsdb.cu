@@ -13,7 +13,9 @@
 // flushed with fp32 vector reductions into workspace accumulators (several
 // CTAs share a tile or an n block); finalize_bwd1 then scales and rounds
 // them (dSq = bf16(alpha/(1-p) dS), dB = bf16(dB^T) transposed) and clears
-// the accumulators, which start every call at zero.
+// the accumulators, which start every call at zero.  At padded ranks up to 32
+// two CTAs share an SM (two stages each): the pass is bound by the one thread
+// per CTA that issues the small MMAs, not by the SM's tensor core.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -24,7 +26,7 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kDyBytes = 2u * 128u * 128u;   // 128 tokens x 128 n
 
-__global__ void __launch_bounds__(kThreads, 1) dsdb_kernel(const __grid_constant__ DsDbParams p) {
+__global__ void __launch_bounds__(kThreads, 2) dsdb_kernel(const __grid_constant__ DsDbParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
