@@ -18,8 +18,9 @@
  * (seed low word, seed high word) and counter (t, j/8, 0, 0): the four
  * output words give eight 16-bit lanes, low half first, and the element is
  * kept iff lane >= T, T = floor(p*65536 + 0.5).  The backward regenerates
- * the decisions from the seed; nothing is stored between the calls except
- * S_saved.
+ * the decisions from the seed, so the calls need share nothing but S_saved;
+ * a caller may instead keep the bits the forward writes (mask_bits) and hand
+ * them to the backward, which then reads them (same decisions, less work).
  *
  * Multi-adapter form (LoRAFusion notes, section 5 "FusedMultiLoRA"; article
  * section 4.1): rows are grouped in 128-row tiles; a segment table assigns
