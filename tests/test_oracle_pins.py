@@ -341,6 +341,72 @@ def test_multi_backward_on_row_subsets_adds_up():
         np.testing.assert_allclose(dB_sum[i], dB[i], rtol=1e-10, atol=1e-10)
 
 
+def multi_fd_mismatch(backward, seed=5):
+    """Central differences of L = sum(dY * Y) through the packed multi-adapter forward, w.r.t. a sample of X
+    entries (rows of both adapters and of the uncovered tail) and every entry of each A_i and B_i.  L is linear
+    in each of them, so h = 1 is exact.  Returns the first gradient that disagrees with `backward`, or None."""
+    rng = np.random.default_rng(seed)
+    k, n = 8, 6
+    adapters = [dict(A=rand(rng, k, r, scale=0.4), B=rand(rng, r, n, scale=0.4), alpha=a, p=pp)
+                for r, a, pp in ((2, 1.5, 0.3), (3, 2.0, 0.0), (2, 0.5, 0.5))]
+    m = 128 + 128 + 7
+    segments = [(0, 128, 1), (128, 128, 0)]          # rows 256..262 have no adapter; adapter 2 owns no rows
+    X, W, dY = rand(rng, m, k), rand(rng, k, n, scale=0.3), rand(rng, m, n)
+    seed_mask = 2**36 + 11
+
+    def loss(Xv, ads):
+        return float((dY * O.multi_lora_forward(Xv, W, ads, segments, seed_mask)[0]).sum())
+
+    dX, dA, dB = backward(dY, X, W, adapters, segments, seed_mask)[:3]
+
+    def central(bump):
+        plus, minus = bump(1.0), bump(-1.0)
+        return (loss(*plus) - loss(*minus)) / 2.0
+
+    for t, j in [(0, 0), (5, 7), (127, 3), (128, 1), (200, 6), (255, 2), (256, 4), (262, 0)]:
+        def bump(h, t=t, j=j):
+            Xh = X.copy()
+            Xh[t, j] += h
+            return Xh, adapters
+        if abs(central(bump) - dX[t, j]) > 1e-9 * max(1.0, abs(dX[t, j])):
+            return "dX"
+    for i in range(len(adapters)):
+        for name, grad in (("A", dA[i]), ("B", dB[i])):
+            for idx in np.ndindex(*grad.shape):
+                def bump(h, i=i, name=name, idx=idx):
+                    ads = [dict(a) for a in adapters]
+                    mat = ads[i][name].copy()
+                    mat[idx] += h
+                    ads[i][name] = mat
+                    return X, ads
+                if abs(central(bump) - grad[idx]) > 1e-9 * max(1.0, abs(grad[idx])):
+                    return f"d{name}{i}"
+    return None
+
+
+def test_multi_gradients_match_finite_differences():
+    """The packed backward against central differences of the packed forward itself, independent of the
+    single-adapter backward: each dA_i / dB_i collects exactly its own rows, with its own alpha and p."""
+    assert multi_fd_mismatch(O.multi_lora_backward) is None
+
+
+def test_multi_finite_differences_catch_misrouted_gradients():
+    """Planted in the oracle's output: adapter 0's one tile counted twice in its dB, or its dA scaled by
+    adapter 1's alpha in place of its own.  The finite-difference pin must reject both."""
+    def tile_twice_in_dB(*args):
+        dX, dA, dB, dS, owner = O.multi_lora_backward(*args)
+        dB = [2.0 * dB[0]] + list(dB[1:])
+        return dX, dA, dB, dS, owner
+
+    def wrong_alpha(*args):
+        dX, dA, dB, dS, owner = O.multi_lora_backward(*args)
+        dA = [dA[0] * (2.0 / 1.5)] + list(dA[1:])
+        return dX, dA, dB, dS, owner
+
+    assert multi_fd_mismatch(tile_twice_in_dB) is not None
+    assert multi_fd_mismatch(wrong_alpha) is not None
+
+
 def test_tile_table_brute_force():
     segments = [(0, 128, 1), (256, 256, 0), (512, 128, 3)]
     tiles = O.tile_adapters(segments, 700, 4)
