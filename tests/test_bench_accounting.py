@@ -66,3 +66,15 @@ def test_product_path_fails_loudly_without_the_library(tmp_path):
             "    print('raised', 'missing' in str(e))\n") % (ROOT, str(tmp_path / "absent.so"))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=120)
     assert r.stdout.strip() == "raised True", r.stdout + r.stderr
+
+
+def test_default_workload_is_the_70b_up_proj_rank_64(bench):
+    # the largest single-GPU layer of the set is the headline: m=16384, k=8192, n=28672, r=64
+    assert bench.DEFAULT_WORKLOAD == "llama70b_up_r64"
+    wl = bench.Workload(bench.DEFAULT_WORKLOAD)
+    M, K, N, R = 16384, 8192, 28672, 64
+    assert (wl.m, wl.parts[0].k, wl.parts[0].n, wl.parts[0].r_max) == (M, K, N, R)
+    assert wl.layer_flops() == 4 * M * K * N + 6 * M * R * (K + N)
+    fwd = M * K + K * N + M * N + K * R + R * N + M * R
+    bwd = M * N + K * N + 2 * M * K + M * R + 2 * (K * R + R * N)
+    assert wl.layer_bytes() == 2 * (fwd + bwd)
