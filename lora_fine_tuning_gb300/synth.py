@@ -200,3 +200,14 @@ def decoder_layer_inputs(seed: int, m: int, r: int):
 MULTI_WORKLOAD = dict(k=8192, n=8192, total_rows=16384, seed=3,
                       specs=[AdapterSpec(16, 1.0, 0.0), AdapterSpec(16, 2.0, 0.1),
                              AdapterSpec(32, 2.0, 0.1), AdapterSpec(64, 4.0, 0.05)])
+
+
+# The rank sweep on a square 4096 layer in its four-adapter form: every adapter at the swept rank, the
+# multi-adapter workload's scales {1, 2, 2, 4}, drop rate 0.1 for all, lognormal sample lengths packed to
+# the swept token count.
+MULTI_SWEEP_WORKLOAD = dict(k=4096, n=4096, seed=4, alphas=(1.0, 2.0, 2.0, 4.0), p=0.1)
+
+
+def multi_sweep_specs(r: int) -> list:
+    """Adapter settings of the four-adapter sweep at rank r."""
+    return [AdapterSpec(r, a, MULTI_SWEEP_WORKLOAD["p"]) for a in MULTI_SWEEP_WORKLOAD["alphas"]]

@@ -6,7 +6,10 @@ by default, and the 8B case also runs the saved-mask mode (bench.py
 --saved-mask: the forward writes the keep bits and the backward reads them).  The
 oracle computes, in fp64 on the host: the full keep mask, S, dS-derived dA and
 dB (all O(m r (k + n))), and Y / dX on a sample of rows (256 random rows plus
-two whole 128-row tiles), which it computes one row at a time.
+two whole 128-row tiles), which it computes one row at a time.  The cases are
+every single-adapter layer of the benchmark set, two decoder-layer projections
+whose shapes the set lacks, the packed four-adapter batch and the largest
+point of the four-adapter rank sweep.
 """
 import numpy as np
 import pytest
@@ -32,11 +35,23 @@ def sample_rows(m, seed):
     return np.array(sorted(rows))
 
 
-@pytest.mark.parametrize("name,saved", [("llama8b_up", False), ("llama8b_up", True), ("llama70b_o_r64", False),
+@pytest.mark.parametrize("name,saved", [("llama8b_up", False), ("llama8b_up", True), ("llama70b_o_r16", False),
+                                        ("llama70b_o_r64", False), ("llama70b_up_r16", False),
                                         ("llama70b_up_r64", False)])   # the largest layer of the benchmark set
 def test_single_adapter_full_size(name, saved):
     cfg = synth.WORKLOADS[name]
-    m, k, n, r, alpha, p, seed = (cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed"))
+    check_single(*(cfg[x] for x in ("m", "k", "n", "r", "alpha", "p", "seed")), saved)
+
+
+# two projections of the Llama-3.1-8B decoder layer whose shapes no other case covers: down_proj (k > n, the
+# backward GEMM's K is only 4096 while its N is 14336) and k_proj (n = 1024: eight column blocks)
+@pytest.mark.parametrize("label,k,n,seed", [("down_proj", 14336, 4096, 11), ("k_proj", 4096, 1024, 6)])
+def test_decoder_layer_projection_full_size(label, k, n, seed):
+    cfg = synth.LAYER_WORKLOAD
+    check_single(cfg["m"], k, n, cfg["r"], cfg["alpha"], cfg["p"], seed, False)
+
+
+def check_single(m, k, n, r, alpha, p, seed, saved):
     raw = synth.layer_inputs(seed, m, k, n, r)
     X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
     ws = api.workspace(m, k, n, r)
@@ -70,8 +85,17 @@ def test_single_adapter_full_size(name, saved):
 
 def test_multi_adapter_full_size():
     w = synth.MULTI_WORKLOAD
-    k, n, seed, specs = w["k"], w["n"], w["seed"], w["specs"]
-    batch = synth.packed_batch(seed, w["total_rows"], len(specs))
+    check_multi(w["k"], w["n"], w["seed"], w["specs"], w["total_rows"])
+
+
+def test_multi_adapter_sweep_point_full_size():
+    """The four-adapter sweep at its largest point: 32768 packed rows, every adapter at rank 128, k = n = 4096."""
+    w = synth.MULTI_SWEEP_WORKLOAD
+    check_multi(w["k"], w["n"], w["seed"], synth.multi_sweep_specs(128), 32768)
+
+
+def check_multi(k, n, seed, specs, total_rows):
+    batch = synth.packed_batch(seed, total_rows, len(specs))
     raw = synth.multi_inputs(seed, k, n, specs, batch)
     X, W, dY = (to_dev(raw[x]) for x in ("X", "W", "dY"))
     adapters = [api.Adapter(A=to_dev(A), B=to_dev(B), alpha=s.alpha, p=s.p) for (A, B), s in zip(raw["adapters"], specs)]
