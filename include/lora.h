@@ -103,8 +103,8 @@ typedef struct {
 size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters);
 
 /* Forward, one adapter.  Writes Y (m x n), S_saved (m x r: alpha * S in bf16,
- * opaque state for lora_bwd) and, if mask_bits is not NULL, the keep
- * decisions: bit j%8 of byte t*(k/8) + j/8.
+ * opaque state for lora_bwd) and, if mask_bits is not NULL (16-byte
+ * aligned, m x k/8 bytes), the keep decisions: bit j%8 of byte t*(k/8) + j/8.
  * Steps (article section 4.1, forward ① and ②): dropout fused with the
  * down-projection, then X W + alpha S B as one contraction [X | alpha S][W; B]. */
 lora_status lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
@@ -154,7 +154,10 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
  *     ||W_j||^2 + 2 alpha B_j . (W^T A)_j + alpha^2 B_j^T (A^T A) B_j,
  * never from the dense k x n update.  Single adapter; rank, p, alignment and
  * shape rules as for lora_fwd.  mag, w_norm2, g_saved and dmag are fp32
- * vectors of n, 16-byte aligned. */
+ * vectors of n, 16-byte aligned.  Every mag_j must be finite and nonzero:
+ * dora_bwd recovers dmag from Y by dividing by mag_j (Y's column j is zero
+ * when mag_j is, and the gradient could not be recovered from it); the
+ * library does not read mag on the host, so it cannot check this. */
 
 /* Workspace bytes for dora_fwd / dora_bwd: lora_workspace_size(m, k, n, r, 1)
  * plus the DoRA accumulators (W^T A, A^T A, dmag).  Same contract as the LoRA
@@ -200,13 +203,14 @@ lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
  *  - Sizes whose scratch need (lora_workspace_size(m, k, n, r, 1)) exceeds
  *    8 MiB are rejected with LORA_EWORKSPACE and lora_last_error_string()
  *    says why.  For example m = 8192, k = 4096, n = 14336, r = 16 needs 2 MB.
- *  - The first call on each device looks up the array's device address and
- *    clears its status word, on `stream`; make that first call before any
- *    stream capture.
+ *  - Arguments are checked exactly as lora_fwd checks them, and before
+ *    anything is enqueued: a call that returns an error has enqueued nothing.
+ *  - The first successful call on each device looks up the array's device
+ *    address and clears the whole array, on `stream`; make that first call
+ *    before any stream capture.
  *  - Every call on a device shares the one array and leaves its contents
- *    behind.  The first call on a device clears the whole array; every call
- *    that completes leaves its accumulators and counters at zero again, so
- *    the next call starts clean.  Calls whose work can overlap on the GPU
+ *    behind.  Every call that completes leaves its accumulators and counters
+ *    at zero again, so the next call (of any shape) starts clean.  Calls whose work can overlap on the GPU
  *    (different streams, no ordering) race on the array.
  *  - Bounded-wait timeouts are recorded in the array's status word, which no
  *    entry point reads back; a call that timed out may leave the array dirty,

@@ -372,7 +372,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         for (int a = 0; a < nad; ++a) {
             const int rp = c.rpads[a];
-            if (!make_map(&p.mapA[a], ads[a].A, ads[a].rank, k, ads[a].rank, std::min(rp, 64), 64,
+            if (!make_map(&p.mapA[a], ads[a].A, ads[a].rank, k, ads[a].rank, std::min(rp, 64), 128,
                           rank_swizzle_host(rp)))
                 return LORA_ECUDA;
         }
@@ -384,12 +384,12 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         p.m = m;
         p.k = k;
         p.ld = c.s_ld;
-        p.nkb = static_cast<int32_t>((k + 63) / 64);
+        p.nkb = static_cast<int32_t>((k + 127) / 128);
         p.units = static_cast<int64_t>(c.rt.n_active) * p.nkb;
         p.seed_lo = seed_lo;
         p.seed_hi = seed_hi;
-        p.stage_bytes = 16384u + 128u * static_cast<uint32_t>(c.rt.rpad_max);
-        p.stages = mask_ring_stages(p.stage_bytes, 12);
+        p.stage_bytes = 32768u + 256u * static_cast<uint32_t>(c.rt.rpad_max);
+        p.stages = mask_ring_stages(p.stage_bytes, 8);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
         LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));
@@ -475,6 +475,12 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         // with the full ring.
         const bool two_per_sm = 2u * p.stage_bytes <= kStageBudget / 2 - 2048;
         p.stages = two_per_sm ? 2 : static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
+        // From padded rank 64 on, the strip order: TMEM of a CTA (512 columns) holds two dS buffers and one
+        // dB^T accumulator per n-block of a strip, each rpad_max columns wide, so dB^T is flushed once per
+        // strip segment instead of once per unit.  Below that, the tile order with per-unit dB^T flushes is
+        // faster (measured on the Llama-3.1-8B up-proj and the m = 16384 square 4096 layer): its flushes are
+        // small, and two CTAs per SM need the TMEM the strip's accumulators would take.
+        p.strip = rpm >= 64 ? std::max(1, std::min<int>(p.nnb, 512 / static_cast<int>(rpm) - 2)) : 0;
         const int64_t ctas = static_cast<int64_t>(two_per_sm ? 2 : 1) * c.sms;
         const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
         LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
@@ -668,7 +674,8 @@ lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_ad
                            int64_t n, lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits, void* workspace,
                            size_t workspace_bytes, void* stream) {
     if (!W || (m > 0 && (!X || !Y))) return LORA_EINVAL;
-    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved)) return LORA_EALIGN;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved) || !aligned16(mask_bits))
+        return LORA_EALIGN;
     if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
     std::lock_guard<std::mutex> lock(g_call_mu);
     static Call c;
@@ -717,11 +724,28 @@ lora_status lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
 lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A, const lora_bf16* B,
                                     float alpha, float p, uint64_t seed, int64_t m, int64_t k, int64_t n, int32_t r,
                                     lora_bf16* Y, lora_bf16* S_saved, uint8_t* mask_bits, void* stream) {
+    // Every check lora_fwd makes comes first, so that a call that fails enqueues nothing (not even the
+    // first call's clearing of the array) and reports the same status lora_fwd would.
+    if (!W || (m > 0 && (!X || !Y || !S_saved))) return LORA_EINVAL;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved) || !aligned16(mask_bits))
+        return LORA_EALIGN;
+    lora_status st = check_dims(m, k, n);
+    if (st) return st;
+    const lora_adapter ad{r, alpha, p, A, B, nullptr, nullptr};
+    st = check_adapter(ad, false);
+    if (st) return st;
+    if ((m + kTileM - 1) / kTileM > kMaxTiles) return LORA_ESHAPE;
     const size_t need = lora_workspace_size(m, k, n, r, 1);
     if (need > kStaticScratchBytes) {
         g_last_error = "lora_fwd_static_scratch: these sizes need more scratch than the 8 MiB static buffer";
         return LORA_EWORKSPACE;
     }
+    int sms = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_call_mu);
+        st = device_setup(&sms);
+    }
+    if (st) return st;
     int dev = 0;
     if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 64) return LORA_ECUDA;
     void* scratch = nullptr;
@@ -870,7 +894,7 @@ lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
                      size_t workspace_bytes, void* stream) {
     if (!W || !mag || !w_norm2 || !g_saved || (m > 0 && (!X || !Y || !S_saved))) return LORA_EINVAL;
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved) || !aligned16(mag) ||
-        !aligned16(w_norm2) || !aligned16(g_saved))
+        !aligned16(w_norm2) || !aligned16(g_saved) || !aligned16(mask_bits))
         return LORA_EALIGN;
     lora_adapter ad{r, alpha, p, A, B, nullptr, nullptr};
     lora_segment seg{0, m, 0, 0};

@@ -42,12 +42,27 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) 
     return done != 0;
 }
 
+// The same, suspending the thread for up to kWaitSuspendNs while the phase is open.
+__device__ __forceinline__ bool mbar_try_wait_cl_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(kWaitSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
 static __device__ __noinline__ bool mbar_wait_cl_slow(uint32_t bar, uint32_t parity, const WaitCtx& w, int site) {
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait_cl(bar, parity)) return true;
+        for (int i = 0; i < 4; ++i)
+            if (mbar_try_wait_cl_sleep(bar, parity)) return true;
         if (*w.abort) return false;
         if (global_timer_ns() - t0 > w.limit_ns) {
             *w.abort = 1;
@@ -68,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait_cl(uint64_t* bar, uint32_t parity, con
 static __device__ __noinline__ bool mbar_wait_cl_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait_cl(a, parity))
+    while (!mbar_try_wait_cl_sleep(a, parity))
         if (global_timer_ns() - t0 > limit_ns) return false;
     return true;
 }

@@ -65,6 +65,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
+// Waits that find their phase still open suspend the thread in hardware for
+// up to this long (it wakes as soon as the phase completes): a role that only
+// waits (the TMA producer, the MMA issuer, an idle mask group) then takes no
+// issue slots from the warps that share its scheduler.
+constexpr uint32_t kWaitSuspendNs = 20000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitSuspendNs)
+        : "memory");
+    return done != 0;
+}
+
 // Per-CTA failure state for bounded waits.  `abort` lives in shared memory;
 // once any thread of the CTA times out, every later wait returns false at
 // once and the roles wind down.
@@ -79,8 +99,8 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     const uint64_t t0 = global_timer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 4; ++i)
+            if (mbar_try_wait_sleep(bar, parity)) return true;
         if (*w.abort) return false;
         if (global_timer_ns() - t0 > w.limit_ns) {
             *w.abort = 1;
@@ -102,7 +122,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
 // TMEM is released).  Gives up after limit_ns.
 static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity))
+    while (!mbar_try_wait_sleep(bar, parity))
         if (global_timer_ns() - t0 > limit_ns) return false;
     return true;
 }
@@ -385,7 +405,8 @@ __device__ __forceinline__ uint32_t carry_mask(uint32_t carry) {
     return m;
 }
 
-// The two keep bits of keep_carry (bit 0: low lane, bit 1: high lane).
+// The two keep bits of keep_carry, or of an AND mask (bits 15 and 31 mark the
+// lanes that keep in both): bit 0 the low lane, bit 1 the high lane.
 __device__ __forceinline__ uint32_t carry_bits(uint32_t carry) { return ((carry >> 15) & 1u) | ((carry >> 30) & 2u); }
 
 // Zeroes the dropped elements of a packed bf16 pair: the low 15 bits of both
@@ -399,6 +420,60 @@ __device__ __forceinline__ uint32_t apply_keep_fast(uint32_t data, uint32_t w, c
     asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(carry));
     return data & m;
 }
+
+// The keep test lane >= T in one of two exact forms, picked per adapter.
+//  - half form, for 1 <= T <= 0x7BFF (drop rates up to 0.484): a lane whose
+//    top bit is set keeps (it is >= 0x8000 > T); any other lane, read as an
+//    IEEE half, is a positive number, +inf or a NaN, and keeps iff it compares
+//    greater-or-equal-or-unordered with T read as a half: finite positive
+//    halves order like their bit patterns, and +inf and every NaN pattern lie
+//    above 0x7BFF.  One f16x2 compare (set.geu gives 0xFFFF per true half)
+//    and one byte permute that spreads each lane's top bit.
+//  - carry form (keep_carry), for every other T.
+struct KeepForm {
+    KeepTest kt;       // carry form constants
+    uint32_t TT;       // T in both 16-bit halves (half form)
+    bool half;
+};
+
+__device__ __forceinline__ KeepForm keep_form(uint32_t T) {
+    KeepForm f;
+    f.kt = keep_test(T);
+    f.TT = T * 0x10001u;
+    f.half = T >= 1u && T <= 0x7BFFu;
+    return f;
+}
+
+// AND mask of one Philox word: 0xFFFF over each 16-bit lane that keeps.
+template <bool kHalf>
+__device__ __forceinline__ uint32_t keep_word_mask(uint32_t w, const KeepForm& f) {
+    uint32_t m;
+    if (kHalf) {
+        uint32_t ge;
+        asm("set.geu.u32.f16x2 %0, %1, %2;" : "=r"(ge) : "r"(w), "r"(f.TT));
+        asm("prmt.b32 %0, %1, 0, 0xBB99;" : "=r"(m) : "r"(w));
+        m |= ge;
+    } else {
+        m = carry_mask(keep_carry(w, f.kt));
+    }
+    return m;
+}
+
+// AND masks of the eight features of one Philox call (row t, counter word g).
+template <bool kHalf>
+__device__ __forceinline__ uint4 keep_chunk_mask(const PhiloxRow& R, uint32_t g, const PhiloxKeys& K,
+                                                 const KeepForm& f) {
+    const uint4 w = philox_10_row(R, g, K);
+    return make_uint4(keep_word_mask<kHalf>(w.x, f), keep_word_mask<kHalf>(w.y, f), keep_word_mask<kHalf>(w.z, f),
+                      keep_word_mask<kHalf>(w.w, f));
+}
+
+// The eight keep bits of a chunk's AND masks (bit e = element e).
+__device__ __forceinline__ uint32_t chunk_mask_bits(uint4 m) {
+    return carry_bits(m.x) | (carry_bits(m.y) << 2) | (carry_bits(m.z) << 4) | (carry_bits(m.w) << 6);
+}
+
+__device__ __forceinline__ uint4 and4(uint4 v, uint4 m) { return make_uint4(v.x & m.x, v.y & m.y, v.z & m.z, v.w & m.w); }
 
 // AND mask of 32-bit word w (elements 2w, 2w + 1) of a 16-byte chunk whose
 // eight keep bits are the low byte of `bits` (bit e = element e).

@@ -80,15 +80,17 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     uint64_t* masked = bars + S;
     uint64_t* empty = bars + 2 * S;
     uint64_t* acc_full = bars + 3 * S;
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* drain = acc_empty + 2;
+    uint64_t* acc_empty = acc_full + kGroups;
+    uint64_t* drain = acc_empty + kGroups;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rpad_max = p.rt.rpad_max;
-    const uint32_t tmem_cols = static_cast<uint32_t>(2 * rpad_max) < 32u ? 32u : static_cast<uint32_t>(2 * rpad_max);
+    // one accumulator buffer per mask group (see the epilogue)
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(kGroups * rpad_max)) tmem_cols <<= 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             mbar_init(&masked[s], kGroupThreads);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kGroups; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], 128);
         }
@@ -173,9 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 const bool first = (u == u0) || d.ti == 0;
                 const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
-                const uint32_t b = use & 1u;
+                const uint32_t b = use % kGroups;
                 if (first) {
-                    if (!mbar_wait(&acc_empty[b], ((use >> 1) & 1u) ^ 1u, w, 2)) break;
+                    if (!mbar_wait(&acc_empty[b], ((use / kGroups) & 1u) ^ 1u, w, 2)) break;
                     tc_fence_after();
                 }
                 if (!mbar_wait(&masked[s], ph, w, 3)) break;
@@ -200,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
     } else {
         // mask warps: group g takes the units u0 + g, u0 + g + kGroups, ...; in
         // it thread -> token row covers the row's 16 chunks (8 per 64-feature
-        // box).  The group that masks a run's last stage also runs its epilogue
+        // box).  Each group also runs the epilogue of every kGroups-th run
         // (TMEM lane quadrant = warp % 4; each group has one warp per quadrant).
         const int mt = threadIdx.x - 64;
         const int group = mt / kGroupThreads;
@@ -218,63 +220,77 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
             const bool last = (u == u1 - 1) || d.ti == d.n_a - 1;
             const bool mine = turn == group;
             if (++turn == kGroups) turn = 0;
-            if (!mine) {
-                if (last) ++use;
-                if (++s == S) { s = 0; ph ^= 1u; }
-                continue;
-            }
             const AdapterDev ad = p.rt.ad[d.a];
-            bool ok = mbar_wait(&full[s], ph, w, 4);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            if (ad.T != 0u && p.use_bits) {
-                // the forward's keep bits: byte cc of the row's 16 covers chunk cc (bit e = feature 8 cc + e)
-                const uint32_t sbase = smem_u32(smem + s * p.stage_bytes);
-                const uint32_t xrow = sbase + row * 128;
-                const uint4 kb4 = lds128(sbase + p.off_bits + row * 16);
-                const uint32_t kw[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
-#pragma unroll
-                for (int cc = 0; cc < kChunks; ++cc) {
-                    const uint32_t byte = kw[cc >> 2] >> (8 * (cc & 3));
-                    const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
-                    uint4 v = lds128(addr);
-                    v.x &= keep_mask_word(byte, 0);
-                    v.y &= keep_mask_word(byte, 1);
-                    v.z &= keep_mask_word(byte, 2);
-                    v.w &= keep_mask_word(byte, 3);
-                    sts128(addr, v);
-                }
-            } else if (ad.T != 0u) {
-                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
+            if (mine) {
+                const bool regen = ad.T != 0u && !p.use_bits;
                 const uint32_t t = static_cast<uint32_t>(static_cast<int64_t>(d.tile) * kTileM + row);
                 const uint32_t g0 = static_cast<uint32_t>(d.fb * 16);
-                if (t != prow_t) {
-                    prow_t = t;
-                    prow = philox_row(t, keys);
-                }
-                const KeepTest kt = keep_test(ad.T);
+                const KeepForm kf = keep_form(ad.T);
+                // The first batch of keep masks depends only on (seed, row, feature): it is computed before
+                // the wait on the stage's data, so that the Philox arithmetic overlaps the TMA load.
+                uint4 km[kBatch];
+                if (regen) {
+                    if (t != prow_t) {
+                        prow_t = t;
+                        prow = philox_row(t, keys);
+                    }
+                    if (kf.half) {
 #pragma unroll
-                for (int c0 = 0; c0 < kChunks; c0 += kBatch) {
-                    uint4 wv[kBatch];
+                        for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<true>(prow, g0 + i, keys, kf);
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < kBatch; ++i) wv[i] = philox_10_row(prow, g0 + c0 + i, keys);
-#pragma unroll
-                    for (int i = 0; i < kBatch; ++i) {
-                        const int cc = c0 + i;                      // chunk of the row: box cc / 8, chunk cc % 8
-                        const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
-                        uint4 v = lds128(addr);
-                        v.x = apply_keep_fast(v.x, wv[i].x, kt);
-                        v.y = apply_keep_fast(v.y, wv[i].y, kt);
-                        v.z = apply_keep_fast(v.z, wv[i].z, kt);
-                        v.w = apply_keep_fast(v.w, wv[i].w, kt);
-                        sts128(addr, v);
+                        for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<false>(prow, g0 + i, keys, kf);
                     }
                 }
+                bool ok = mbar_wait(&full[s], ph, w, 4);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                if (ad.T != 0u && p.use_bits) {
+                    // the forward's keep bits: byte cc of the row's 16 covers chunk cc (bit e = feature 8 cc + e)
+                    const uint32_t sbase = smem_u32(smem + s * p.stage_bytes);
+                    const uint32_t xrow = sbase + row * 128;
+                    const uint4 kb4 = lds128(sbase + p.off_bits + row * 16);
+                    const uint32_t kw[4] = {kb4.x, kb4.y, kb4.z, kb4.w};
+#pragma unroll
+                    for (int cc = 0; cc < kChunks; ++cc) {
+                        const uint32_t byte = kw[cc >> 2] >> (8 * (cc & 3));
+                        const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
+                        uint4 v = lds128(addr);
+                        v.x &= keep_mask_word(byte, 0);
+                        v.y &= keep_mask_word(byte, 1);
+                        v.z &= keep_mask_word(byte, 2);
+                        v.w &= keep_mask_word(byte, 3);
+                        sts128(addr, v);
+                    }
+                } else if (regen) {
+                    const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
+#pragma unroll
+                    for (int c0 = 0; c0 < kChunks; c0 += kBatch) {
+                        if (c0 > 0) {
+                            if (kf.half) {
+#pragma unroll
+                                for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<true>(prow, g0 + c0 + i, keys, kf);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<false>(prow, g0 + c0 + i, keys, kf);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) {
+                            const int cc = c0 + i;                      // chunk of the row: box cc / 8, chunk cc % 8
+                            const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
+                            sts128(addr, and4(lds128(addr), km[i]));
+                        }
+                    }
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&masked[s]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&masked[s]);
-            if (last) {
-                const uint32_t b = use & 1u;
-                ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
+            // The epilogue of run e is run by group e % kGroups, which is also the TMEM buffer the run
+            // accumulated in: each buffer is waited on by one group only, in order, so a parity wait never
+            // meets a phase two behind, however many tiles each adapter's runs have.
+            const uint32_t b = use % kGroups;
+            if (last && b == static_cast<uint32_t>(group)) {
+                const bool ok = mbar_wait(&acc_full[b], (use / kGroups) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
                 const int64_t j = static_cast<int64_t>(d.fb) * 128 + quad * 32 + lane;
@@ -294,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
-                ++use;
             }
+            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }
@@ -354,7 +370,7 @@ __global__ void stuck_wait_kernel(DevCtl ctl) {
 
 }  // namespace
 
-size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 5) * 8 + 16; }
+size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 2 * kGroups + 1) * 8 + 16; }
 
 cudaError_t da_configure() {
     return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);

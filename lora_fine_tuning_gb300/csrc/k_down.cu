@@ -3,21 +3,22 @@
 // LoRAFusion notes (papers.chlience.com), section 5 "FusedLoRA": dropout and
 // the down-projection are one pass so the full-size X is read once; the
 // article (juhe.plus) section 4.1 lists it as forward step ①.  Here:
-//  - warp 0 streams X tiles (128 x 64, TMA, 128B swizzle) and the matching
-//    64-row block of A_a into a ring of shared-memory stages;
+//  - warp 0 streams X tiles (128 rows x 128 features: two TMA boxes, 128B
+//    swizzle) and the matching 128-row block of A_a into a ring of
+//    shared-memory stages;
 //  - warps 2..9 regenerate the keep mask with Philox4x32-10 and zero the
 //    dropped elements in place (16 bytes = 8 features = one Philox call per
 //    access), then hand the stage to the MMA warp.  They form two groups of
 //    four warps that take alternate stages, and a thread owns one whole row
-//    of its stage: eight independent Philox calls per thread and stage, with
-//    the counter's row word shared.  The Philox rounds are a chain of
-//    dependent multiplies, so it is the independent calls in flight per
-//    scheduler that set the mask rate;
-//  - warp 1 issues tcgen05.mma (M = 128 tokens, N = rank, K = 64 per stage)
-//    into a double-buffered TMEM accumulator;
-//  - at the end of each tile range, the group that masked its last stage
-//    reads TMEM and adds the fp32 partial into S_acc with vector reductions (ranges of one tile may be
-//    split over CTAs: units are spread evenly, stream-K style).
+//    of its stage: sixteen Philox calls per thread and stage, eight at a
+//    time, with the counter's row word shared.  The first eight are computed
+//    before the wait on the stage's data;
+//  - warp 1 issues tcgen05.mma (M = 128 tokens, N = rank, K = 128 per stage)
+//    into TMEM, one accumulator buffer per mask group;
+//  - at the end of each tile range the group that owns the range's buffer
+//    reads TMEM and adds the fp32 partial into S_acc with vector reductions
+//    (ranges of one tile may be split over CTAs: units are spread evenly,
+//    stream-K style).
 // finalize_s then applies alpha/(1-p), writes S' in bf16 and clears S_acc,
 // which starts every call at zero.
 #include "common.cuh"
@@ -32,11 +33,47 @@ constexpr int kMaskThreads = 32 * kMaskWarps;
 constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
 constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
 constexpr int kGroups = kMaskGroups;               // mask groups, taking stages in turn (S % kGroups == 0)
-constexpr int kParts = kGroupThreads / 128;        // group threads per tile row
-constexpr int kChunks = 8 / kParts;                // 16-byte chunks (8 features) per thread and stage
-static_assert(kChunks == 8, "a thread owns a whole 64-feature row of its stage");
+constexpr int kChunks = 16;                        // 16-byte chunks (8 features) of a row per stage: two 64-feature boxes
+constexpr int kBatch = 8;                          // Philox calls computed before their chunks are masked
 static_assert(kGroupThreads == 128, "a group is four warps: one thread per tile row, one warp per TMEM lane quadrant");
-constexpr uint32_t kXBytes = 128u * 128u;   // 128 rows x 64 bf16; then 64 rows of A (rpad_max x 2 bytes each)
+constexpr uint32_t kXBytes = 2u * 128u * 128u;   // 128 rows x 128 bf16 (two boxes); then 128 rows of A (rpad_max x 2 B each)
+
+// The sixteen keep-bit bytes of a row's k-block (byte cc = chunk cc) to the caller's buffer: one 16-byte
+// store when k is a multiple of 128, else byte by byte up to k.
+__device__ __forceinline__ void store_row_bits(uint8_t* dst, uint4 v, int kb, int64_t k) {
+    if ((k & 127) == 0) {
+        *reinterpret_cast<uint4*>(dst) = v;
+    } else {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i)
+            if ((static_cast<int64_t>(kb) * kChunks + i) * 8 < k) dst[i] = static_cast<uint8_t>(w[i >> 2] >> (8 * (i & 3)));
+    }
+}
+
+// Zeroes the dropped elements of one thread's row of a stage (16 chunks; the first kBatch keep masks come
+// in `km`, computed before the data arrived), and with kBits also writes the row's keep bits.
+template <bool kHalf, bool kBits>
+__device__ __forceinline__ void apply_row(uint32_t xrow, int row, const PhiloxRow& prow, uint32_t g0,
+                                          const PhiloxKeys& keys, const KeepForm& kf, uint4 (&km)[kBatch],
+                                          uint8_t* bits, int kb, int64_t k) {
+    uint32_t kw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int c0 = 0; c0 < kChunks; c0 += kBatch) {
+        if (c0 > 0) {
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<kHalf>(prow, g0 + c0 + i, keys, kf);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int cc = c0 + i;                  // chunk of the row: box cc / 8, chunk cc % 8
+            const uint32_t addr = xrow + (cc >> 3) * 16384 + (((cc & 7) ^ (row & 7)) << 4);
+            sts128(addr, and4(lds128(addr), km[i]));
+            if (kBits) kw[cc >> 2] |= chunk_mask_bits(km[i]) << (8 * (cc & 3));
+        }
+    }
+    if (kBits) store_row_bits(bits, make_uint4(kw[0], kw[1], kw[2], kw[3]), kb, k);
+}
 
 __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_constant__ DownParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -52,15 +89,17 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     uint64_t* masked = bars + S;
     uint64_t* empty = bars + 2 * S;
     uint64_t* acc_full = bars + 3 * S;
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* drain = acc_empty + 2;
+    uint64_t* acc_empty = acc_full + kGroups;
+    uint64_t* drain = acc_empty + kGroups;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     __shared__ int abort_flag;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int rpad_max = p.rt.rpad_max;
-    const uint32_t tmem_cols = static_cast<uint32_t>(2 * rpad_max) < 32u ? 32u : static_cast<uint32_t>(2 * rpad_max);
+    // one accumulator buffer per mask group (see the epilogue)
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>(kGroups * rpad_max)) tmem_cols <<= 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -68,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             mbar_init(&masked[s], kGroupThreads);
             mbar_init(&empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kGroups; ++b) {
             mbar_init(&acc_full[b], 1);
             mbar_init(&acc_empty[b], kGroupThreads);
         }
@@ -107,10 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 const int rpad = p.rt.ad[a].rpad;
                 if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                 uint8_t* xs = smem + s * p.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], kXBytes + 128u * static_cast<uint32_t>(rpad));
-                tma_load_2d(xs, &p.mapX, &full[s], kb * 64, tile * kTileM);
-                tma_load_2d(xs + kXBytes, &p.mapA[a], &full[s], 0, kb * 64);
-                if (rpad > 64) tma_load_2d(xs + kXBytes + 8192, &p.mapA[a], &full[s], 64, kb * 64);
+                mbar_arrive_expect_tx(&full[s], kXBytes + 256u * static_cast<uint32_t>(rpad));
+                tma_load_2d(xs, &p.mapX, &full[s], kb * 128, tile * kTileM);
+                tma_load_2d(xs + 16384, &p.mapX, &full[s], kb * 128 + 64, tile * kTileM);
+                tma_load_2d(xs + kXBytes, &p.mapA[a], &full[s], 0, kb * 128);
+                if (rpad > 64) tma_load_2d(xs + kXBytes + 16384, &p.mapA[a], &full[s], 64, kb * 128);
                 ++issued;
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
@@ -141,24 +181,26 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                     cur_rpad = rpad;
                     idesc = make_idesc_bf16(128, rpad, false, true);
                     rb = rank_row_bytes(rpad);
-                    a_d0 = make_smem_desc(sbase + kXBytes, 8192, 8 * rb, rank_swizzle(rpad));   // A_a rows, MN-major
+                    a_d0 = make_smem_desc(sbase + kXBytes, 16384, 8 * rb, rank_swizzle(rpad));   // A_a rows, MN-major
                 }
                 const bool first = (u == u0) || kb == 0;
                 const bool last = (u == u1 - 1) || kb == p.nkb - 1;
-                const uint32_t b = use & 1u;
+                const uint32_t b = use % kGroups;
                 if (first) {
-                    if (!mbar_wait(&acc_empty[b], ((use >> 1) & 1u) ^ 1u, w, 2)) break;
+                    if (!mbar_wait(&acc_empty[b], ((use / kGroups) & 1u) ^ 1u, w, 2)) break;
                     tc_fence_after();
                 }
                 if (!mbar_wait(&masked[s], ph, w, 3)) break;
                 tc_fence_after();
                 const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
                 const uint32_t d = tmem + b * static_cast<uint32_t>(rpad_max);
-                // 16 features per step: 32 B of the X row, 16 rows (16 * rb B) of A_a
+                // 16 features per step: 32 B of the X row in box ks / 4, 16 rows (16 * rb B) of A_a
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16(d, x_d0 + so + ks * 2u, a_d0 + so + static_cast<uint64_t>(ks) * rb, idesc,
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t xo = static_cast<uint64_t>(ks >> 2) * 1024u + static_cast<uint64_t>(ks & 3) * 2u;
+                    umma_bf16(d, x_d0 + so + xo, a_d0 + so + static_cast<uint64_t>(ks) * rb, idesc,
                               (first && ks == 0) ? 0u : 1u);
+                }
                 umma_commit(&empty[s]);
                 if (last) {
                     umma_commit(&acc_full[b]);
@@ -173,9 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
     } else {
         // mask warps: group g takes the units u0 + g, u0 + g + kGroups, ...; in
         // it thread -> row covers the row's kChunks 16-byte chunks, so the
-        // Philox counter word is the row for all of them.  The group that
-        // masks a tile range's last stage also runs its epilogue (TMEM lane
-        // quadrant = warp % 4; each group has one warp per quadrant).
+        // Philox counter word is the row for all of them.  Each group also
+        // runs the epilogue of every kGroups-th tile range (TMEM lane quadrant
+        // = warp % 4; each group has one warp per quadrant).
         const int mt = threadIdx.x - 64;
         const int group = mt / kGroupThreads;
         const int row = mt & 127;
@@ -193,64 +235,59 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
             const bool last = (u == u1 - 1) || kb == p.nkb - 1;
             const bool mine = turn == group;
             if (++turn == kGroups) turn = 0;
-            if (!mine) {
-                if (last) ++use;
-                if (++s == S) { s = 0; ph ^= 1u; }
-                continue;
-            }
             const int tile = it.tile;
             const int a = it.a;
-            const uint32_t T = p.rt.ad[a].T;
-            bool ok = mbar_wait(&full[s], ph, w, 4);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
-            uint32_t kbyte[kChunks];     // keep bits of each chunk (bit e = feature 8 (kb * 8 + i) + e)
-            if (T != 0u) {
-                const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
-                if (static_cast<uint32_t>(t) != prow_t) {
-                    prow_t = static_cast<uint32_t>(t);
-                    prow = philox_row(prow_t, keys);
+            if (mine) {
+                const uint32_t T = p.rt.ad[a].T;
+                const int64_t t = static_cast<int64_t>(tile) * kTileM + row;
+                // The first batch of keep masks depends only on (seed, row, feature): it is computed before
+                // the wait on the stage's data, so that the Philox arithmetic overlaps the TMA load.
+                uint4 km[kBatch];
+                const KeepForm kf = keep_form(T);
+                const uint32_t g0 = static_cast<uint32_t>(kb * kChunks);
+                if (T != 0u) {
+                    if (static_cast<uint32_t>(t) != prow_t) {
+                        prow_t = static_cast<uint32_t>(t);
+                        prow = philox_row(prow_t, keys);
+                    }
+                    if (kf.half) {
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<true>(prow, g0 + i, keys, kf);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kBatch; ++i) km[i] = keep_chunk_mask<false>(prow, g0 + i, keys, kf);
+                    }
                 }
-                uint4 wv[kChunks];
-#pragma unroll
-                for (int i = 0; i < kChunks; ++i)
-                    wv[i] = philox_10_row(prow, static_cast<uint32_t>(kb * 8 + i), keys);
-                const KeepTest kt = keep_test(T);
-#pragma unroll
-                for (int i = 0; i < kChunks; ++i) {
-                    const uint32_t addr = xrow + ((i ^ (row & 7)) << 4);
-                    uint4 v = lds128(addr);
-                    const uint32_t c0 = keep_carry(wv[i].x, kt), c1 = keep_carry(wv[i].y, kt);
-                    const uint32_t c2 = keep_carry(wv[i].z, kt), c3 = keep_carry(wv[i].w, kt);
-                    v.x &= carry_mask(c0);
-                    v.y &= carry_mask(c1);
-                    v.z &= carry_mask(c2);
-                    v.w &= carry_mask(c3);
-                    sts128(addr, v);
-                    kbyte[i] = carry_bits(c0) | (carry_bits(c1) << 2) | (carry_bits(c2) << 4) | (carry_bits(c3) << 6);
+                bool ok = mbar_wait(&full[s], ph, w, 4);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                if (T != 0u) {
+                    const uint32_t xrow = smem_u32(smem + s * p.stage_bytes) + row * 128;
+                    // the keep bits are packed only when the caller keeps them (it costs a quarter of the
+                    // mask arithmetic)
+                    uint8_t* bits = (p.mask_bits != nullptr && t < p.m)
+                                        ? p.mask_bits + t * (p.k >> 3) + static_cast<int64_t>(kb) * kChunks
+                                        : nullptr;
+                    if (bits == nullptr) {
+                        if (kf.half) apply_row<true, false>(xrow, row, prow, g0, keys, kf, km, nullptr, 0, 0);
+                        else apply_row<false, false>(xrow, row, prow, g0, keys, kf, km, nullptr, 0, 0);
+                    } else {
+                        if (kf.half) apply_row<true, true>(xrow, row, prow, g0, keys, kf, km, bits, kb, p.k);
+                        else apply_row<false, true>(xrow, row, prow, g0, keys, kf, km, bits, kb, p.k);
+                    }
+                } else if (p.mask_bits != nullptr && t < p.m) {
+                    // p = 0 keeps everything: all bits set
+                    uint8_t* bits = p.mask_bits + t * (p.k >> 3) + static_cast<int64_t>(kb) * kChunks;
+                    store_row_bits(bits, make_uint4(~0u, ~0u, ~0u, ~0u), kb, p.k);
                 }
-            } else {
-#pragma unroll
-                for (int i = 0; i < kChunks; ++i) kbyte[i] = 0xFFu;
+                fence_proxy_async_smem();
+                mbar_arrive(&masked[s]);
             }
-            if (p.mask_bits != nullptr && t < p.m) {
-                uint8_t* dst = p.mask_bits + t * (p.k >> 3) + static_cast<int64_t>(kb) * 8;
-                if ((p.k & 63) == 0) {
-                    // the row's eight bytes of this k-block in one aligned 8-byte store
-                    const uint32_t lo = kbyte[0] | (kbyte[1] << 8) | (kbyte[2] << 16) | (kbyte[3] << 24);
-                    const uint32_t hi = kbyte[4] | (kbyte[5] << 8) | (kbyte[6] << 16) | (kbyte[7] << 24);
-                    *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < kChunks; ++i)
-                        if ((static_cast<int64_t>(kb) * 8 + i) * 8 < p.k) dst[i] = static_cast<uint8_t>(kbyte[i]);
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&masked[s]);
-            if (last) {
-                const uint32_t b = use & 1u;
-                ok = mbar_wait(&acc_full[b], (use >> 1) & 1u, w, 5);
+            // The epilogue of tile range e is run by group e % kGroups, which is also the TMEM buffer the
+            // range accumulated in: each buffer is waited on by one group only, in order, so a parity wait
+            // never meets a phase two behind, whatever the lengths of the ranges.
+            const uint32_t b = use % kGroups;
+            if (last && b == static_cast<uint32_t>(group)) {
+                const bool ok = mbar_wait(&acc_full[b], (use / kGroups) & 1u, w, 5);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
                 const AdapterDev ad = p.rt.ad[a];
@@ -271,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_con
                 }
                 tc_fence_before();
                 mbar_arrive(&acc_empty[b]);
-                ++use;
             }
+            if (last) ++use;
             if (++s == S) { s = 0; ph ^= 1u; }
         }
     }
@@ -307,7 +344,7 @@ __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ 
 }  // namespace
 
 size_t down_smem_bytes(const DownParams& p) {
-    return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (3 * p.stages + 5) * 8 + 16;
+    return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (3 * p.stages + 2 * kGroups + 1) * 8 + 16;
 }
 
 cudaError_t down_configure() {

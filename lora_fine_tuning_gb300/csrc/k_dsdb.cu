@@ -8,14 +8,28 @@
 // Each unit is one (128-row tile, 128-wide n block) of dY, staged by TMA as two
 // 128B-swizzled 128 x 64 boxes.  The same shared-memory tile is read twice by
 // the tensor cores: K-major for dS (K = n) and MN-major for dB^T (M = n,
-// K = tokens).  dS accumulates in TMEM over a CTA's run of n blocks of one
-// tile; dB^T is produced per unit in a double-buffered accumulator.  Both are
-// flushed with fp32 vector reductions into workspace accumulators (several
-// CTAs share a tile or an n block); finalize_bwd1 then scales and rounds
-// them (dSq = bf16(alpha/(1-p) dS), dB = bf16(dB^T) transposed) and clears
-// the accumulators, which start every call at zero.  At padded ranks up to 32
-// two CTAs share an SM (two stages each): the pass is bound by the one thread
-// per CTA that issues the small MMAs, not by the SM's tensor core.
+// K = tokens).
+//
+// Both products reduce over a different dimension of dY (dS over n, dB over
+// the tokens), so whichever accumulator a CTA cannot keep must be flushed
+// with fp32 reductions.  Two orders of the units:
+//  - tile order (padded rank <= 32): tile by tile, each tile's n-blocks in
+//    order.  dS stays in TMEM over the CTA's run of n-blocks and every unit's
+//    128 x r dB^T partial is flushed.  At these ranks the flushes are small,
+//    and two CTAs share each SM (two stages each): the small MMAs are bound by
+//    the one thread per CTA that issues them, not by the SM's tensor core.
+//  - strip order (padded rank >= 64), where per-unit dB^T flushes would move
+//    as many bytes as dY itself.  Units are walked in strips of `strip`
+//    n-blocks; inside a strip, tile after tile in routing order, each tile's
+//    n-blocks innermost.  TMEM holds one dB^T accumulator per n-block of the
+//    strip for as long as the CTA stays in the strip with one adapter (a
+//    segment), and a double-buffered dS accumulator per tile visit.  Per unit
+//    of dY the reductions are then 128 x r floats divided by the strip width
+//    (dS), plus one flush of the strip's dB^T accumulators per segment: at
+//    rank 64 a sixth of the bytes of the tile order.
+// Either way finalize_bwd1 then scales and rounds the sums (dSq =
+// bf16(alpha/(1-p) dS), dB = bf16(dB^T) transposed) and clears the
+// accumulators, which start every call at zero.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -26,7 +40,54 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kDyBytes = 2u * 128u * 128u;   // 128 tokens x 128 n
 
-__global__ void __launch_bounds__(kThreads, 2) dsdb_kernel(const __grid_constant__ DsDbParams p) {
+// Walks units from u0 on in strip order (strip s of width w, active tile slot,
+// n-block j of the strip), without a division per unit.  Every role of the
+// kernel walks the same sequence with its own copy.
+struct StripIter {
+    int s, slot, j, w, tile, a;
+    int J, nnb, n_active;
+    __device__ __forceinline__ StripIter(int64_t u0, int J_, int nnb_, const Routing& rt)
+        : J(J_), nnb(nnb_), n_active(rt.n_active) {
+        const int64_t per = static_cast<int64_t>(n_active) * J;
+        const int last = (nnb - 1) / J;
+        s = static_cast<int>(u0 / per);
+        if (s > last) s = last;
+        w = min(J, nnb - s * J);
+        const int64_t rem = u0 - static_cast<int64_t>(s) * per;
+        slot = static_cast<int>(rem / w);
+        j = static_cast<int>(rem - static_cast<int64_t>(slot) * w);
+        load(rt);
+    }
+    __device__ __forceinline__ void load(const Routing& rt) {
+        if (slot < n_active) {
+            tile = rt.active_tiles[slot];
+            a = rt.tile_adapter[tile];
+        }
+    }
+    __device__ __forceinline__ int nb() const { return s * J + j; }
+    // this unit is the last of its segment (strip and adapter) in the walk order
+    __device__ __forceinline__ bool segment_ends(const Routing& rt) const {
+        if (j != w - 1) return false;
+        if (slot + 1 >= n_active) return true;
+        return rt.tile_adapter[rt.active_tiles[slot + 1]] != a;
+    }
+    __device__ __forceinline__ void next(const Routing& rt) {
+        if (++j == w) {
+            j = 0;
+            if (++slot == n_active) {
+                slot = 0;
+                ++s;
+                w = min(J, nnb - s * J);
+            }
+            load(rt);
+        }
+    }
+};
+
+// Tile order (padded rank <= 32): units walked tile by tile, each tile's n-blocks
+// in order; dS accumulates in TMEM over the CTA's run of n-blocks of a tile and
+// each unit's dB^T partial is flushed from a double-buffered accumulator.
+__global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_constant__ DsDbParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
@@ -244,6 +305,242 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_kernel(const __grid_constant
     }
 }
 
+// Strip order (padded rank >= 64), described at the top of this file.
+__global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_constant__ DsDbParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const int S = p.stages;
+    const int J = p.strip;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;
+    uint64_t* accS_full = bars + 2 * S;     // [2]
+    uint64_t* accS_empty = accS_full + 2;   // [2]
+    uint64_t* accB_full = accS_empty + 2;
+    uint64_t* accB_empty = accB_full + 1;
+    uint64_t* drain = accB_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rpad_max = p.rt.rpad_max;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>((2 + J) * rpad_max)) tmem_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accS_full[b], 1);
+            mbar_init(&accS_empty[b], 128);
+        }
+        mbar_init(accB_full, 1);
+        mbar_init(accB_empty, 128);
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapDY);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem;                                                   // dS: two buffers
+    const uint32_t tB = tmem + 2u * static_cast<uint32_t>(rpad_max);            // dB^T: one per n-block of a strip
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDsDb << 8};
+
+    const int64_t U = p.units;
+    const int64_t u0 = U * blockIdx.x / gridDim.x;
+    const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+    const uint32_t bbox = static_cast<uint32_t>(rpad_max) * 128u;   // spacing of the two B boxes
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            StripIter it(u0, J, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int nb = it.nb();
+                const int tile = it.tile;
+                const int a = it.a;
+                const int rpad = p.rt.ad[a].rpad;
+                if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                uint8_t* st = smem + s * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], kDyBytes + 2u * 128u * rpad + 256u * rpad);
+                tma_load_2d(st, &p.mapDY, &full[s], nb * 128, tile * kTileM);
+                tma_load_2d(st + 16384, &p.mapDY, &full[s], nb * 128 + 64, tile * kTileM);
+                tma_load_2d(st + p.off_b, &p.mapB[a], &full[s], nb * 128, 0);
+                tma_load_2d(st + p.off_b + bbox, &p.mapB[a], &full[s], nb * 128 + 64, 0);
+                tma_load_2d(st + p.off_s, &p.mapS[a], &full[s], 0, tile * kTileM);
+                if (rpad > 64) tma_load_2d(st + p.off_s + 16384, &p.mapS[a], &full[s], 64, tile * kTileM);
+                ++issued;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t visits = 0, segs = 0, used = 0;
+            bool new_seg = true;
+            // Operand descriptors of stage 0, built once: an MMA only moves the start-address
+            // field (bytes / 16) by its stage and K step.  The rank-dependent ones (N = rpad,
+            // S' layout) are rebuilt when the adapter's padded rank changes.
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t ds_a0 = make_smem_desc(sbase, 16, 1024, kSw128);              // dY, K-major
+            const uint64_t ds_b0 = make_smem_desc(sbase + p.off_b, 16, 1024, kSw128);    // B_a, K-major
+            const uint64_t db_a0 = make_smem_desc(sbase, 16384, 1024, kSw128);           // dY^T, MN-major
+            const uint32_t bbox16 = bbox >> 4;
+            int cur_rpad = -1;
+            uint32_t idesc_s = 0, idesc_b = 0, rb = 0;
+            uint64_t db_b0 = 0;
+            StripIter it(u0, J, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int rpad = p.rt.ad[it.a].rpad;
+                if (rpad != cur_rpad) {
+                    cur_rpad = rpad;
+                    idesc_s = make_idesc_bf16(128, rpad, false, false);
+                    idesc_b = make_idesc_bf16(128, rpad, true, true);
+                    rb = rank_row_bytes(rpad);
+                    db_b0 = make_smem_desc(sbase + p.off_s, 16384, 8u * rb, rank_swizzle(rpad));   // S', MN-major
+                }
+                const bool visit_first = (u == u0) || it.j == 0;
+                const bool visit_last = (u == u1 - 1) || it.j == it.w - 1;
+                const bool seg_last = (u == u1 - 1) || it.segment_ends(p.rt);
+                if (new_seg) {
+                    // the previous segment's dB^T accumulators have been flushed
+                    if (!mbar_wait(accB_empty, (segs & 1u) ^ 1u, w, 2)) break;
+                    tc_fence_after();
+                    used = 0;
+                }
+                const uint32_t bs = visits & 1u;
+                if (visit_first) {
+                    if (!mbar_wait(&accS_empty[bs], ((visits >> 1) & 1u) ^ 1u, w, 3)) break;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&full[s], ph, w, 4)) break;
+                tc_fence_after();
+                const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
+                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
+                const uint32_t dS_acc = tS + bs * static_cast<uint32_t>(rpad_max);
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
+                    umma_bf16(dS_acc, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
+                              (visit_first && ks == 0) ? 0u : 1u);
+                }
+                // dB^T[n-block] (+)= dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens,
+                // N = rpad): 16 tokens per step = 2048 B of dY and 16 * rb B of S'
+                const uint32_t dB_acc = tB + static_cast<uint32_t>(it.j * rpad_max);
+                const bool fresh = ((used >> it.j) & 1u) == 0u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
+                              (fresh && ks == 0) ? 0u : 1u);
+                used |= 1u << it.j;
+                umma_commit(&empty[s]);
+                if (visit_last) {
+                    umma_commit(&accS_full[bs]);
+                    ++visits;
+                }
+                new_seg = seg_last;
+                if (seg_last) {
+                    umma_commit(accB_full);
+                    ++segs;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else {
+        const int quad = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t visits = 0, segs = 0, used = 0;
+        StripIter it(u0, J, p.nnb, p.rt);
+        for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+            const AdapterDev ad = p.rt.ad[it.a];
+            const bool visit_last = (u == u1 - 1) || it.j == it.w - 1;
+            const bool seg_last = (u == u1 - 1) || it.segment_ends(p.rt);
+            used |= 1u << it.j;
+            if (visit_last) {
+                const uint32_t bs = visits & 1u;
+                const bool ok = mbar_wait(&accS_full[bs], (visits >> 1) & 1u, w, 5);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                const int64_t row = static_cast<int64_t>(it.tile) * kTileM + quad * 32 + lane;
+                float* dst = p.dS_acc + row * p.ld;
+                const uint32_t taddr = tS + lane_off + bs * static_cast<uint32_t>(rpad_max);
+                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + c0, v);
+                    tmem_ld_wait();
+                    if (row < p.m) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                           __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&accS_empty[bs]);
+                ++visits;
+            }
+            if (seg_last) {
+                const bool ok = mbar_wait(accB_full, segs & 1u, w, 6);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                for (int jj = 0; jj < it.w; ++jj) {
+                    if (!((used >> jj) & 1u)) continue;
+                    const int64_t nidx = static_cast<int64_t>(it.s * J + jj) * 128 + quad * 32 + lane;
+                    float* dst = p.acc_base + ad.dB_off + nidx * ad.rpad;
+                    const uint32_t taddr = tB + lane_off + static_cast<uint32_t>(jj * rpad_max);
+                    for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + c0, v);
+                        tmem_ld_wait();
+                        if (nidx < p.n) {
+#pragma unroll
+                            for (int q = 0; q < 16; q += 4)
+                                if (c0 + q < ad.rank)
+                                    red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                               __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(accB_empty);
+                ++segs;
+                used = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
 // dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0, on
 // rows of active tiles (parts & kPartDs); dB_a[c, j] = bf16(dB^T_acc_a[j, c])
 // (parts & kPartDb).  Every accumulator read is cleared.
@@ -331,11 +628,14 @@ __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict
 size_t dsdb_smem_bytes(const DsDbParams& p) { return 1024 + p.stages * p.stage_bytes + (2 * p.stages + 7) * 8 + 16; }
 
 cudaError_t dsdb_configure() {
-    return cudaFuncSetAttribute(dsdb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    const cudaError_t e = cudaFuncSetAttribute(dsdb_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(dsdb_strip_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
-    return launch_pdl(dsdb_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
+    if (p.strip > 0) return launch_pdl(dsdb_strip_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
+    return launch_pdl(dsdb_tile_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
 }
 
 cudaError_t launch_finalize_bwd1(const DsDbParams& p, int parts, int sms, cudaStream_t stream, bool pdl) {

@@ -50,10 +50,10 @@ struct DevCtl {
 };
 
 // Down-projection: S_acc[t, c] += sum_j (X .* D)[t, j] A_a[j, c] over stream-K
-// ranges of (active tile, 64-wide k-block) units.
+// ranges of (active tile, 128-wide k-block) units.
 struct DownParams {
     CUtensorMap mapX;                  // X: dims {k, m}, box {64, 128}, 128B swizzle
-    CUtensorMap mapA[kMaxAdapters];    // A_i: dims {r_i, k}, box {min(rpad,64), 64}, swizzle by rpad
+    CUtensorMap mapA[kMaxAdapters];    // A_i: dims {r_i, k}, box {min(rpad,64), 128}, swizzle by rpad
     Routing rt;
     DevCtl ctl;
     float* S_acc;                      // m x ld fp32 (zero on entry; cleared by finalize_s)
@@ -61,11 +61,11 @@ struct DownParams {
     uint8_t* mask_bits;                // optional, m x k/8
     int64_t m, k;
     int32_t ld;                        // s_ld
-    int32_t nkb;                       // ceil(k / 64)
+    int32_t nkb;                       // ceil(k / 128)
     int64_t units;                     // n_active * nkb
     uint32_t seed_lo, seed_hi;
     int32_t stages;
-    uint32_t stage_bytes;              // X tile (16 KB) + 64 rows of A (128 * rpad_max bytes)
+    uint32_t stage_bytes;              // X tile (two 16 KB boxes) + 128 rows of A (256 * rpad_max bytes)
 };
 
 // CTA-pair GEMM with the rank-r tail (k_gemm2.cu).
@@ -90,8 +90,13 @@ struct GemmParams {
 };
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,
-//   acc_dS[tile]  += dY_tile B_a^T        (accumulated over the item's n-blocks)
-//   acc_dBt[nblk]  = dY_tile^T S'_tile    (flushed per unit)
+//   acc_dS[tile]  += dY_tile B_a^T
+//   acc_dBt[nblk] += dY_tile^T S'_tile
+// strip == 0 (tile order): units tile by tile, n-blocks in order; dS is kept in
+// TMEM over a CTA's run of n-blocks, each unit's dB^T is flushed.  strip > 0:
+// units strip by strip (strip = `strip` consecutive n-blocks), tiles in routing
+// order inside a strip, n-blocks innermost; dS is flushed per tile visit and a
+// strip's dB^T accumulators stay in TMEM while the CTA stays in the strip.
 struct DsDbParams {
     CUtensorMap mapDY;                 // dY {n, m}, box {64, 128}, 128B swizzle
     CUtensorMap mapB[kMaxAdapters];    // B_i {n, r_i}, box {64, rpad}, 128B swizzle (K-major, K = n)
@@ -105,6 +110,7 @@ struct DsDbParams {
     int64_t m, n;
     int32_t ld;
     int32_t nnb;                       // ceil(n / 128)
+    int32_t strip;                     // 0: tile order; else n-blocks per strip (one dB^T accumulator each in TMEM)
     int64_t units;                     // n_active * nnb
     int32_t stages;
     uint32_t stage_bytes, off_b, off_s; // stage layout

@@ -190,6 +190,25 @@ def test_maximum_rows_and_adapters():
     check_multi(k, n, segments, raw, specs, seed, adapters, Y, S, mask, dX)
 
 
+@pytest.mark.parametrize("tiles", [(1, 2, 1, 3), (1, 1, 1, 1, 2, 1, 3, 1)])
+def test_adapters_with_few_tiles(tiles):
+    """Adapters that own one to three tiles and many 128-feature blocks: the dA pass then runs many short
+    runs of mixed lengths, so consecutive runs end on different mask groups; each run's partial must
+    still be read after its own MMAs only.  Adapters alternate in row order."""
+    k, n, seed = 2048, 256, 43
+    specs = [synth.AdapterSpec((16, 32, 16, 64)[i % 4], (1.0, 2.0, 0.5, 4.0)[i % 4], (0.1, 0.05, 0.2, 0.1)[i % 4])
+             for i in range(len(tiles))]
+    segments, row = [], 0
+    for a, t in enumerate(tiles):
+        segments.append((row, 128 * t, a))
+        row += 128 * t
+    batch = synth.PackedBatch(m=row, segments=segments, valid=[rows for _, rows, _ in segments])
+    raw = synth.multi_inputs(seed, k, n, specs, batch)
+    for _ in range(3):     # the race it guards against depends on timing: run it a few times
+        adapters, Y, S, mask, dX = run_multi(k, n, segments, raw, specs, seed)
+        check_multi(k, n, segments, raw, specs, seed, adapters, Y, S, mask, dX)
+
+
 def test_routing_table_matches_oracle():
     batch = synth.packed_batch(3, 16384, 4)
     from lora_fine_tuning_gb300 import native
