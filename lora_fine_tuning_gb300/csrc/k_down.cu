@@ -28,11 +28,9 @@ namespace lora {
 
 namespace {
 
-constexpr int kMaskWarps = 4 * kMaskGroups;        // warps 2.. mask, and run the epilogue
-constexpr int kMaskThreads = 32 * kMaskWarps;
-constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
+// Warps 2.. mask (and run the epilogue) in G groups of four; warp 0 is the TMA producer, warp 1 the MMA issuer.
 constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
-constexpr int kGroups = kMaskGroups;               // mask groups, taking stages in turn (S % kGroups == 0)
+constexpr int threads_of(int groups) { return 64 + kGroupThreads * groups; }
 constexpr int kChunks = 16;                        // 16-byte chunks (8 features) of a row per stage: two 64-feature boxes
 constexpr int kBatch = 8;                          // Philox calls computed before their chunks are masked
 static_assert(kGroupThreads == 128, "a group is four warps: one thread per tile row, one warp per TMEM lane quadrant");
@@ -75,7 +73,10 @@ __device__ __forceinline__ void apply_row(uint32_t xrow, int row, const PhiloxRo
     if (kBits) store_row_bits(bits, make_uint4(kw[0], kw[1], kw[2], kw[3]), kb, k);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) down_proj_kernel(const __grid_constant__ DownParams p) {
+// G mask groups take the ring's stages in turn (S % G == 0).
+template <int G>
+__global__ void __launch_bounds__(threads_of(G), 1) down_proj_kernel(const __grid_constant__ DownParams p) {
+    constexpr int kGroups = G;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
@@ -344,15 +345,21 @@ __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ 
 }  // namespace
 
 size_t down_smem_bytes(const DownParams& p) {
-    return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (3 * p.stages + 2 * kGroups + 1) * 8 + 16;
+    return 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + (3 * p.stages + 2 * p.groups + 1) * 8 + 16;
 }
 
 cudaError_t down_configure() {
-    return cudaFuncSetAttribute(down_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    cudaError_t e = cudaFuncSetAttribute(down_proj_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(down_proj_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(down_proj_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    return e;
 }
 
 cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
-    return launch_pdl(down_proj_kernel, dim3(grid), dim3(kThreads), down_smem_bytes(p), stream, p);
+    if (p.groups == 4) return launch_pdl(down_proj_kernel<4>, dim3(grid), dim3(threads_of(4)), down_smem_bytes(p), stream, p);
+    if (p.groups == 3) return launch_pdl(down_proj_kernel<3>, dim3(grid), dim3(threads_of(3)), down_smem_bytes(p), stream, p);
+    if (p.groups == 2) return launch_pdl(down_proj_kernel<2>, dim3(grid), dim3(threads_of(2)), down_smem_bytes(p), stream, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream) {

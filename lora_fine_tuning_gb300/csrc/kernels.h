@@ -45,15 +45,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 constexpr int kMaxDynSmem = 225 * 1024;
 // Stage ring budget of the rank-r kernels (stages * stage bytes).
 constexpr int kStageBudget = 220 * 1024;
-// down_proj and da mask their stages in kMaskGroups groups of four warps that take the ring's stages in
-// turn.  Their rings hold a multiple of kMaskGroups stages, so that every stage belongs to one group: a group
-// then never waits on a stage another group may still be working through, and a parity wait can never see
-// the completion of a phase two behind.
+// down_proj and da mask their stages in groups of four warps that take the ring's stages in turn.  Their
+// rings hold a multiple of the group count, so that every stage belongs to one group: a group then never
+// waits on a stage another group may still be working through, and a parity wait can never see the
+// completion of a phase two behind.
 constexpr int kMaskGroups = 2;
 
-inline int mask_ring_stages(size_t stage_bytes, int max_stages) {
+inline int mask_ring_stages(size_t stage_bytes, int max_stages, int groups = kMaskGroups) {
     int s = static_cast<int>(std::min<size_t>(static_cast<size_t>(max_stages), kStageBudget / stage_bytes));
-    return s - s % kMaskGroups;
+    return s - s % groups;
 }
 
 size_t down_smem_bytes(const DownParams& p);

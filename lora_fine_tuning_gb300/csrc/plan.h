@@ -66,6 +66,7 @@ struct DownParams {
     uint32_t seed_lo, seed_hi;
     int32_t stages;
     uint32_t stage_bytes;              // X tile (two 16 KB boxes) + 128 rows of A (256 * rpad_max bytes)
+    int32_t groups;                    // mask groups of four warps (2 or 4); stages % groups == 0
 };
 
 // CTA-pair GEMM with the rank-r tail (k_gemm2.cu).
