@@ -65,6 +65,7 @@ MULTI = "multi_4ad"      # packed batch, four adapters with ranks 16/16/32/64 on
 GREEDY = "multi_4ad_greedy"   # a global batch of the same samples packed into 16384-row microbatches (greedy)
 LAYER = "llama8b_layer"  # the seven LoRA projections of one Llama-3.1-8B decoder layer
 DORA = "dora8b_up"       # the Llama-3.1-8B up-proj layer as DoRA (magnitude per output column)
+MULTI_SQ = "multi_square4096"   # four adapters at one swept rank on a square 4096 weight, packed to --m rows
 
 
 class Part:
@@ -125,12 +126,17 @@ class Workload:
                                                                                                mb0["valid"])])
             self.spec_rows = [sum(-(-l // 128) * 128 for l, a in zip(lengths, ads) if a == i)
                               for i in range(len(specs))]
-        elif name == MULTI:
-            w = synth.MULTI_WORKLOAD
-            specs = [(s.rank, s.alpha, s.p) for s in w["specs"]]
-            batch = synth.packed_batch(w["seed"], m or w["total_rows"], len(specs))
+        elif name in (MULTI, MULTI_SQ):
+            if name == MULTI:
+                w = synth.MULTI_WORKLOAD
+                aspecs, rows = w["specs"], m or w["total_rows"]
+            else:
+                w = synth.MULTI_SWEEP_WORKLOAD
+                aspecs, rows = synth.multi_sweep_specs(r or 16), m or 16384
+            specs = [(s.rank, s.alpha, s.p) for s in aspecs]
+            batch = synth.packed_batch(w["seed"], rows, len(specs))
             self.m = batch.m
-            raw = synth.multi_inputs(w["seed"], w["k"], w["n"], w["specs"], batch)
+            raw = synth.multi_inputs(w["seed"], w["k"], w["n"], aspecs, batch)
             self.owner = np.full(self.m, -1, dtype=np.int64)
             valid = []
             for (start, rows, a), v in zip(batch.segments, batch.valid):
@@ -196,7 +202,7 @@ class Workload:
             return (f"{self.name}: {self.n_samples} samples (lognormal lengths, {self.valid_tokens} tokens) packed "
                     f"first-fit decreasing into {self.n_batches} microbatches of {self.m} rows "
                     f"({self.packed_rows} rows used by tiles), k={q.k}, n={q.n}, adapters {ads}")
-        if self.name == MULTI:
+        if self.name in (MULTI, MULTI_SQ):
             q = self.parts[0]
             ads = ", ".join(f"(r={r}, alpha={a}, p={p})" for r, a, p in q.specs)
             return (f"{self.name}: packed multi-adapter LoRA linear, {self.m} padded rows ({self.n_samples} samples, "
@@ -597,6 +603,20 @@ class DeviceProblem:
         for d in reversed(self.parts):
             self._bwd(d)
 
+    def part_step(self, d):
+        self._fwd(d)
+        self._bwd(d)
+
+    def part_frozen(self, d):
+        api, s = self.api, self.stream
+        api.multi_lora_fwd(d["X"], d["W"], [], [], 0, Y=d["Y"], ws=self.ws, stream=s)
+        api.multi_lora_bwd(d["dY"], d["X"], d["W"], [], [], 0, None, dX=d["dX"], ws=self.ws, stream=s)
+
+    def part_torch(self, d):
+        import torch
+        torch.matmul(d["X"], d["W"], out=d["Y"])
+        torch.matmul(d["dY"], d["W"].t(), out=d["dX"])
+
     def frozen_step(self):
         """The same linears with no adapter: Y = X W and dX = dY W^T through the same GEMM kernels."""
         api, s = self.api, self.stream
@@ -840,6 +860,28 @@ def run_native(args):
                   "lora_overhead_vs_ours": ms_per_step / res["ours"],
                   "lora_overhead_vs_torch": ms_per_step / res["torch_matmul"]}
 
+    # --- per projection (workloads of several linears): each one's fwd+bwd alone, its frozen GEMMs alone ---
+    per_projection = None
+    if wl.name == LAYER and not args.no_frozen:
+        peaks_pp, _ = load_peaks()
+        per_projection = []
+        for d in prob.parts:
+            q = d["part"]
+            t = {}
+            for label, fn in (("lora", prob.part_step), ("frozen_ours", prob.part_frozen),
+                              ("frozen_torch", prob.part_torch)):
+                fn(d)
+                torch.cuda.synchronize(dev)
+                t[label] = max_over_ranks(timed_loop(lambda: fn(d), args.steps, stream, flush)) / args.steps
+            r = q.specs[0][0]
+            flops = 4 * wl.tokens * q.k * q.n + 6 * wl.tokens * r * (q.k + q.n)
+            per_projection.append({
+                "projection": q.label, "k": q.k, "n": q.n, "r": r, "ms_lora": t["lora"],
+                "ms_frozen_ours": t["frozen_ours"], "ms_frozen_torch": t["frozen_torch"],
+                "overhead_vs_ours": t["lora"] / t["frozen_ours"], "overhead_vs_torch": t["lora"] / t["frozen_torch"],
+                "tflops": flops / (t["lora"] / 1e3) / 1e12,
+                "frac_of_measured_peak": flops / (t["lora"] / 1e3) / 1e12 / peaks_pp["bf16_tflops"]})
+
     if rank != 0:
         return
 
@@ -913,6 +955,8 @@ def run_native(args):
         line["sustained"] = sustained
     if frozen:
         line["frozen"] = frozen
+    if per_projection:
+        line["per_projection"] = per_projection
     print(json.dumps(line), flush=True)
 
 
@@ -922,10 +966,12 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS) + [MULTI, GREEDY, LAYER, DORA])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(synth.WORKLOADS) + [MULTI, MULTI_SQ, GREEDY, LAYER, DORA])
     ap.add_argument("--m", type=int, default=None,
                     help="override the workload's token count (padded rows for the packed workload)")
-    ap.add_argument("--r", type=int, default=None, help="override the rank of a single-adapter workload")
+    ap.add_argument("--r", type=int, default=None,
+                    help="override the rank of a single-adapter workload (multi_square4096: every adapter's rank)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline leg")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0)
     ap.add_argument("--no-e2e", action="store_true")

@@ -46,6 +46,15 @@
  *    Every call that completes leaves it zeroed again; after a call reports
  *    LORA_EDEVICE_TIMEOUT, zero it before reusing it.  One workspace must not
  *    be used by two calls that may run concurrently.
+ *  - Host threads may call any entry point at the same time: every call
+ *    prepares its launches in storage of its own thread, and no call holds a
+ *    lock while it enqueues work.  Calls on different streams with different
+ *    workspaces are independent on the GPU too: the backward's side stream
+ *    (below) belongs to the caller's stream.
+ *  - The backward forks its dA pass onto a side stream and joins it back to
+ *    `stream` before it returns work to it.  The first backward call on a
+ *    stream creates that stream's side stream and two events; make it before
+ *    any stream capture.
  */
 #ifndef LORA_GB300_H
 #define LORA_GB300_H

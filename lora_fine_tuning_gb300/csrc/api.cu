@@ -24,11 +24,18 @@ struct DeviceState {
     bool ready = false;
     lora_status status = LORA_OK;
     int sms = 0;
-    // The backward's dA pass runs on `side`, forked from and joined back to the
-    // caller's stream, so that it can use the SMs the dX GEMM's last wave of
-    // tiles leaves idle.
-    cudaStream_t side = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+// The backward's dA pass runs on a side stream, forked from and joined back to
+// the caller's stream, so that it can use the SMs the dX GEMM's last wave of
+// tiles leaves idle.  Each caller stream (per device) gets its own side stream
+// and fork / join events, so that callers on different streams stay
+// independent of one another.
+struct SideStream {
+    int device;
+    cudaStream_t caller;
+    cudaStream_t side;
+    cudaEvent_t fork, join;
 };
 
 std::mutex g_mu;
@@ -105,10 +112,7 @@ lora_status device_setup(int* sms_out) {
             d.sms = sms;
             if (!cuda_ok(down_configure()) || !cuda_ok(gemm2_configure()) ||
                 !cuda_ok(dsdb_configure()) ||
-                !cuda_ok(da_configure()) || !cuda_ok(dora_configure()) ||
-                !cuda_ok(cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking)) ||
-                !cuda_ok(cudaEventCreateWithFlags(&d.fork, cudaEventDisableTiming)) ||
-                !cuda_ok(cudaEventCreateWithFlags(&d.join, cudaEventDisableTiming)))
+                !cuda_ok(da_configure()) || !cuda_ok(dora_configure()))
                 d.status = LORA_ECUDA;
         }
         if (d.status == LORA_OK && g_encode == nullptr) {
@@ -128,14 +132,31 @@ lora_status device_setup(int* sms_out) {
     return LORA_OK;
 }
 
-// The current device's side stream and its fork / join events (device_setup has run).
-void side_stream(cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
+std::vector<SideStream> g_side;   // guarded by g_mu
+
+// The side stream and fork / join events of `caller` on the current device, created on first use (the first
+// backward call on a stream therefore creates a stream and two events: make it before any stream capture).
+bool side_stream(cudaStream_t caller, cudaStream_t* side, cudaEvent_t* fork, cudaEvent_t* join) {
     int dev = 0;
-    cudaGetDevice(&dev);
-    const DeviceState& d = g_dev[dev];
-    *side = d.side;
-    *fork = d.fork;
-    *join = d.join;
+    if (!cuda_ok(cudaGetDevice(&dev))) return false;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (const SideStream& e : g_side)
+        if (e.device == dev && e.caller == caller) {
+            *side = e.side;
+            *fork = e.fork;
+            *join = e.join;
+            return true;
+        }
+    SideStream e{dev, caller, nullptr, nullptr, nullptr};
+    if (!cuda_ok(cudaStreamCreateWithFlags(&e.side, cudaStreamNonBlocking)) ||
+        !cuda_ok(cudaEventCreateWithFlags(&e.fork, cudaEventDisableTiming)) ||
+        !cuda_ok(cudaEventCreateWithFlags(&e.join, cudaEventDisableTiming)))
+        return false;
+    g_side.push_back(e);
+    *side = e.side;
+    *fork = e.fork;
+    *join = e.join;
+    return true;
 }
 
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
@@ -367,7 +388,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     const int nad = c.rt.n_adapters;
 
     if (nad > 0 && c.rt.n_active > 0) {
-        static DownParams p;  // large: keep it off the stack
+        thread_local DownParams p;  // large: off the stack, one per calling thread
         std::memset(&p, 0, sizeof(p));
         if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         for (int a = 0; a < nad; ++a) {
@@ -399,7 +420,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));
     }
 
-    static GemmParams g;
+    thread_local GemmParams g;
     std::memset(&g, 0, sizeof(g));
     if (!make_map(&g.mapA, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
     if (!make_map(&g.mapB, W, n, k, n, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
@@ -428,6 +449,15 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     return LORA_OK;
 }
 
+// Output tile width of the backward (dX) GEMM: 256 columns with one accumulator set (dY W^T and the
+// branch's dSq A^T fill TMEM), or 128 with two sets, so that a tile's epilogue overlaps the next tile's MMAs.
+int bwd_tile_width(int64_t m, int64_t k, int64_t n) {
+    (void)m;
+    (void)k;
+    (void)n;
+    return kBwdPairBN;
+}
+
 lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const uint16_t* W, const lora_adapter* ads,
                     uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, const uint8_t* mask_bits,
                     uint16_t* dX) {
@@ -448,7 +478,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
     }
 
     if (nad > 0 && c.rt.n_active > 0) {
-        static DsDbParams p;
+        thread_local DsDbParams p;
         std::memset(&p, 0, sizeof(p));
         if (!make_map(&p.mapDY, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         for (int a = 0; a < nad; ++a) {
@@ -497,20 +527,21 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     if (fork_da) {
-        side_stream(&side, &ev_fork, &ev_join);
+        if (!side_stream(c.stream, &side, &ev_fork, &ev_join)) return LORA_ECUDA;
         LORA_CUDA(cudaEventRecord(ev_fork, c.stream));
         LORA_CUDA(cudaStreamWaitEvent(side, ev_fork, 0));
     }
 
     if (m > 0) {
-        static GemmParams g;
+        thread_local GemmParams g;
         std::memset(&g, 0, sizeof(g));
         if (!make_map(&g.mapA, dY, n, m, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
-        if (!make_map(&g.mapB, W, n, k, n, 64, kBwdPairBN / 2, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
+        const int bn = bwd_tile_width(m, k, n);
+        if (!make_map(&g.mapB, W, n, k, n, 64, bn / 2, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         if (nad > 0) {
             if (!make_map(&g.mapTA, dsq, c.s_ld, m, c.s_ld, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
             for (int a = 0; a < nad; ++a)
-                if (!make_map(&g.mapTB[a], ads[a].A, ads[a].rank, k, ads[a].rank, 64, kBwdPairBN / 2,
+                if (!make_map(&g.mapTB[a], ads[a].A, ads[a].rank, k, ads[a].rank, 64, bn / 2,
                               CU_TENSOR_MAP_SWIZZLE_128B))
                     return LORA_ECUDA;
         }
@@ -526,11 +557,11 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         g.seed_hi = seed_hi;
         // the forward's keep bits, when given, replace the epilogue's Philox (whole 32-bit words per row)
         g.keep_bits = (mask_bits != nullptr && k % 32 == 0) ? mask_bits : nullptr;
-        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, kBwdPairBN, c.sms, c.stream); }));
+        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
     }
 
     if (fork_da) {
-        static DaParams p;
+        thread_local DaParams p;
         std::memset(&p, 0, sizeof(p));
         if (!make_map(&p.mapX, X, k, m, k, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
         for (int a = 0; a < nad; ++a) {
@@ -585,7 +616,7 @@ lora_status run_dora_norm(const Call& c, const DoraFwd& d, const uint16_t* W, co
     const int r = ad.rank, rp = rank_pad(r);
     const int64_t n_tiles = (k + kTileM - 1) / kTileM;
     if (n_tiles > kMaxTiles) return LORA_ESHAPE;
-    static DaParams pu;
+    thread_local DaParams pu;
     std::memset(&pu, 0, sizeof(pu));
     if (!make_map(&pu.mapX, W, n, k, n, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return LORA_ECUDA;
     if (!make_map(&pu.mapD[0], ad.A, r, k, r, std::min(rp, 64), 128, rank_swizzle_host(rp))) return LORA_ECUDA;
@@ -648,7 +679,6 @@ DoraLayout dora_layout(size_t base, int64_t n, int r) {
     return D;
 }
 
-std::mutex g_call_mu;  // the static parameter blocks above are shared
 
 // Scratch for lora_fwd_static_scratch, for callers that cannot hand the
 // library any device memory of their own.  Every GPU that loads the library
@@ -681,8 +711,7 @@ lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_ad
     if (!aligned16(X) || !aligned16(W) || !aligned16(Y) || !aligned16(S_saved) || !aligned16(mask_bits))
         return LORA_EALIGN;
     if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
-    std::lock_guard<std::mutex> lock(g_call_mu);
-    static Call c;
+    thread_local Call c;
     lora_status st = prepare(c, adapters, n_adapters, segments, n_segments, m, k, n, false, workspace,
                              workspace_bytes, stream);
     if (st) return st;
@@ -698,8 +727,7 @@ lora_status multi_lora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_b
         !aligned16(mask_bits))
         return LORA_EALIGN;
     if (n_adapters > 0 && m > 0 && !S_saved) return LORA_EINVAL;
-    std::lock_guard<std::mutex> lock(g_call_mu);
-    static Call c;
+    thread_local Call c;
     lora_status st = prepare(c, adapters, n_adapters, segments, n_segments, m, k, n, true, workspace,
                              workspace_bytes, stream);
     if (st) return st;
@@ -745,10 +773,7 @@ lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, cons
         return LORA_EWORKSPACE;
     }
     int sms = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_call_mu);
-        st = device_setup(&sms);
-    }
+    st = device_setup(&sms);
     if (st) return st;
     int dev = 0;
     if (!cuda_ok(cudaGetDevice(&dev)) || dev < 0 || dev >= 64) return LORA_ECUDA;
@@ -775,8 +800,7 @@ lora_status lora_tile_table(const lora_segment* segments, int32_t n_segments, in
     if (m < 0 || m > LORA_MAX_ROWS || n_adapters < 0 || n_adapters > kMaxAdapters) return LORA_EINVAL;
     const int64_t need = (m + kTileM - 1) / kTileM;
     if (!tile_adapter || n_tiles < need) return LORA_EINVAL;
-    static int8_t owner[kMaxTiles];
-    std::lock_guard<std::mutex> lock(g_call_mu);
+    thread_local int8_t owner[kMaxTiles];
     lora_status st = tile_table(segments, n_segments, n_adapters, m, owner, need);
     if (st) return st;
     for (int64_t t = 0; t < need; ++t) tile_adapter[t] = owner[t];
@@ -880,11 +904,7 @@ lora_status dora_weight_norm2(const lora_bf16* W, int64_t k, int64_t n, float* w
     if (k <= 0 || n <= 0 || n % 8 || k > LORA_MAX_FEATURES || n > LORA_MAX_FEATURES) return LORA_ESHAPE;
     if (!aligned16(W) || !aligned16(w_norm2)) return LORA_EALIGN;
     int sms = 0;
-    lora_status st;
-    {
-        std::lock_guard<std::mutex> lock(g_call_mu);
-        st = device_setup(&sms);
-    }
+    const lora_status st = device_setup(&sms);
     if (st) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (!cuda_ok(cudaMemsetAsync(w_norm2, 0, static_cast<size_t>(n) * 4, s))) return LORA_ECUDA;
@@ -902,8 +922,7 @@ lora_status dora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_bf16* A,
         return LORA_EALIGN;
     lora_adapter ad{r, alpha, p, A, B, nullptr, nullptr};
     lora_segment seg{0, m, 0, 0};
-    std::lock_guard<std::mutex> lock(g_call_mu);
-    static Call c;
+    thread_local Call c;
     lora_status st = prepare(c, &ad, 1, &seg, m > 0 ? 1 : 0, m, k, n, false, workspace, workspace_bytes, stream);
     if (st) return st;
     const DoraLayout D = dora_layout(c.L.total, n, r);
@@ -930,8 +949,7 @@ lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
         return LORA_EALIGN;
     lora_adapter ad{r, alpha, p, A, B, dA, dB};
     lora_segment seg{0, m, 0, 0};
-    std::lock_guard<std::mutex> lock(g_call_mu);
-    static Call c;
+    thread_local Call c;
     lora_status st = prepare(c, &ad, 1, &seg, m > 0 ? 1 : 0, m, k, n, true, workspace, workspace_bytes, stream);
     if (st) return st;
     const DoraLayout D = dora_layout(c.L.total, n, r);

@@ -161,6 +161,8 @@ WORKLOADS = {
     "llama70b_o_r64": dict(m=16384, k=8192, n=8192, r=64, alpha=2.0, p=0.1, seed=2),
     "llama70b_up_r16": dict(m=16384, k=8192, n=28672, r=16, alpha=2.0, p=0.1, seed=2),
     "llama70b_up_r64": dict(m=16384, k=8192, n=28672, r=64, alpha=2.0, p=0.1, seed=2),
+    # the Llama-3.1-8B MLP down-projection alone (k > n: the backward GEMM's K is n = 4096)
+    "llama8b_down": dict(m=8192, k=14336, n=4096, r=16, alpha=2.0, p=0.1, seed=11),
     # square 4096 layer for sweeps over the token count and the rank
     "square4096": dict(m=4096, k=4096, n=4096, r=16, alpha=2.0, p=0.1, seed=4),
 }
