@@ -449,6 +449,9 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     return LORA_OK;
 }
 
+// Padded rank from which the dS/dB pass walks its units in strip order (see run_bwd).
+constexpr uint32_t kStripMinRank = 32;
+
 // Output tile width of the backward (dX) GEMM: 256 columns with one accumulator set (dY W^T and the
 // branch's dSq A^T fill TMEM), or 128 with two sets, so that a tile's epilogue overlaps the next tile's MMAs.
 int bwd_tile_width(int64_t m, int64_t k, int64_t n) {
@@ -503,18 +506,18 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.off_b = 32768;
         p.off_s = p.off_b + 2 * 128 * rpm;
         p.stage_bytes = p.off_s + 256 * rpm;
-        // Every small MMA of this pass costs its CTA's one issuing thread about 100 cycles, whatever its N.
-        // So when two stages fit in half the shared memory (padded rank <= 32), two CTAs share each SM,
-        // each with a two-stage ring and half the units per issuer.  Larger ranks keep one CTA per SM
-        // with the full ring.
+        // Two issuing threads per CTA (dS and dB^T) share the small MMAs' fixed per-instruction cost.  When
+        // two stages fit in half the shared memory (padded rank <= 32), two CTAs share each SM, each with a
+        // two-stage ring; larger ranks keep one CTA per SM with the deepest ring that fits.
         const bool two_per_sm = 2u * p.stage_bytes <= kStageBudget / 2 - 2048;
         p.stages = two_per_sm ? 2 : static_cast<int32_t>(std::min<size_t>(8, kStageBudget / p.stage_bytes));
-        // From padded rank 64 on, the strip order: TMEM of a CTA (512 columns) holds two dS buffers and one
-        // dB^T accumulator per n-block of a strip, each rpad_max columns wide, so dB^T is flushed once per
-        // strip segment instead of once per unit.  Below that, the tile order with per-unit dB^T flushes is
-        // faster (measured on the Llama-3.1-8B up-proj and the m = 16384 square 4096 layer): its flushes are
-        // small, and two CTAs per SM need the TMEM the strip's accumulators would take.
-        p.strip = rpm >= 64 ? std::max(1, std::min<int>(p.nnb, 512 / static_cast<int>(rpm) - 2)) : 0;
+        // From padded rank 32 on, the strip order: TMEM of a CTA (512 columns, 256 when two CTAs share the
+        // SM) holds two dS buffers and one dB^T accumulator per n-block of a strip, each rpad_max columns
+        // wide, so dB^T is flushed once per strip segment instead of once per unit.  At padded rank 16 the
+        // tile order with per-unit dB^T flushes is faster: its flushes are small.  Measured (us): rank 16 on
+        // the Llama-3.1-8B up-proj 52 tile / 61 strip; rank 32 on the square 4096 layer at m = 16384
+        // 52.3 tile / 46.5 strip, at m = 4096 21.9 tile / 23.7 strip.
+        p.strip = rpm >= kStripMinRank ? std::max(1, std::min<int>(p.nnb, (two_per_sm ? 256 : 512) / static_cast<int>(rpm) - 2)) : 0;
         const int64_t ctas = static_cast<int64_t>(two_per_sm ? 2 : 1) * c.sms;
         const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
         LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));

@@ -13,13 +13,11 @@
 // Both products reduce over a different dimension of dY (dS over n, dB over
 // the tokens), so whichever accumulator a CTA cannot keep must be flushed
 // with fp32 reductions.  Two orders of the units:
-//  - tile order (padded rank <= 32): tile by tile, each tile's n-blocks in
+//  - tile order (padded rank 16): tile by tile, each tile's n-blocks in
 //    order.  dS stays in TMEM over the CTA's run of n-blocks and every unit's
-//    128 x r dB^T partial is flushed.  At these ranks the flushes are small,
-//    and two CTAs share each SM (two stages each): the small MMAs are bound by
-//    the one thread per CTA that issues them, not by the SM's tensor core.
-//  - strip order (padded rank >= 64), where per-unit dB^T flushes would move
-//    as many bytes as dY itself.  Units are walked in strips of `strip`
+//    128 x r dB^T partial is flushed.  At this rank the flushes are small.
+//  - strip order (padded rank >= 32), where per-unit dB^T flushes would move
+//    up to as many bytes as dY itself.  Units are walked in strips of `strip`
 //    n-blocks; inside a strip, tile after tile in routing order, each tile's
 //    n-blocks innermost.  TMEM holds one dB^T accumulator per n-block of the
 //    strip for as long as the CTA stays in the strip with one adapter (a
@@ -27,6 +25,10 @@
 //    of dY the reductions are then 128 x r floats divided by the strip width
 //    (dS), plus one flush of the strip's dB^T accumulators per segment: at
 //    rank 64 a sixth of the bytes of the tile order.
+// In both orders two threads issue the MMAs of a stage (dS and dB^T): a small
+// MMA costs its issuing thread a fixed time whatever its size.  Where two
+// stages fit in half the shared memory (padded rank <= 32) two CTAs share each
+// SM with two-stage rings; otherwise one CTA per SM holds the deepest ring.
 // Either way finalize_bwd1 then scales and rounds the sums (dSq =
 // bf16(alpha/(1-p) dS), dB = bf16(dB^T) transposed) and clears the
 // accumulators, which start every call at zero.
@@ -37,7 +39,7 @@ namespace lora {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;   // warp 0 TMA, warp 1 dS MMA issuer, warps 2-5 epilogue, warp 6 dB MMA issuer
 constexpr uint32_t kDyBytes = 2u * 128u * 128u;   // 128 tokens x 128 n
 
 // Walks units from u0 on in strip order (strip s of width w, active tile slot,
@@ -84,7 +86,7 @@ struct StripIter {
     }
 };
 
-// Tile order (padded rank <= 32): units walked tile by tile, each tile's n-blocks
+// Tile order (padded rank 16): units walked tile by tile, each tile's n-blocks
 // in order; dS accumulates in TMEM over the CTA's run of n-blocks of a tile and
 // each unit's dB^T partial is flushed from a double-buffered accumulator.
 __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_constant__ DsDbParams p) {
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);   // both issuers' commits
         }
         mbar_init(accS_full, 1);
         mbar_init(accS_empty, 128);
@@ -119,7 +121,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
             mbar_init(&accB_full[b], 1);
             mbar_init(&accB_empty[b], 128);
         }
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -173,8 +175,12 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
                     mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
+        // Two issuing threads: warp 1 issues the dS MMAs, warp 6 the dB^T MMAs of the same stage.  A small
+        // MMA costs its issuing thread a fixed time whatever its size, so two issuers halve the issue time
+        // per stage; each commits its own MMAs (a stage is free once both have).
         if (lane == 0) {
+            const bool ds_role = warp == 1;
             int s = 0;
             uint32_t ph = 0;
             uint32_t units_done = 0, items_done = 0;
@@ -202,43 +208,50 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
                 }
                 const bool first = (u == u0) || nb == 0;
                 const bool last = (u == u1 - 1) || nb == p.nnb - 1;
-                if (first) {
-                    if (!mbar_wait(accS_empty, (items_done & 1u) ^ 1u, w, 2)) break;
+                const uint32_t bb = units_done & 1u;
+                if (ds_role) {
+                    if (first) {
+                        if (!mbar_wait(accS_empty, (items_done & 1u) ^ 1u, w, 2)) break;
+                        tc_fence_after();
+                    }
+                } else {
+                    if (!mbar_wait(&accB_empty[bb], ((units_done >> 1) & 1u) ^ 1u, w, 3)) break;
                     tc_fence_after();
                 }
-                const uint32_t bb = units_done & 1u;
-                if (!mbar_wait(&accB_empty[bb], ((units_done >> 1) & 1u) ^ 1u, w, 3)) break;
-                tc_fence_after();
                 if (!mbar_wait(&full[s], ph, w, 4)) break;
                 tc_fence_after();
                 const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
-                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
+                if (ds_role) {
+                    // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
-                    umma_bf16(tS, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
-                              (first && ks == 0) ? 0u : 1u);
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
+                        umma_bf16(tS, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
+                                  (first && ks == 0) ? 0u : 1u);
+                    }
+                    umma_commit(&empty[s]);
+                    if (last) {
+                        umma_commit(accS_full);
+                        ++items_done;
+                    }
+                } else {
+                    // dB^T = dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens, N = rpad):
+                    // 16 tokens per step = 2048 B of dY and 16 * rb B of S'
+                    const uint32_t dB_acc = tB + bb * static_cast<uint32_t>(rpad_max);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
+                                  ks != 0 ? 1u : 0u);
+                    umma_commit(&empty[s]);
+                    umma_commit(&accB_full[bb]);
                 }
-                // dB^T = dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens, N = rpad):
-                // 16 tokens per step = 2048 B of dY and 16 * rb B of S'
-                const uint32_t dB_acc = tB + bb * static_cast<uint32_t>(rpad_max);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
-                              ks != 0 ? 1u : 0u);
-                umma_commit(&empty[s]);
-                umma_commit(&accB_full[bb]);
                 ++units_done;
-                if (last) {
-                    umma_commit(accS_full);
-                    ++items_done;
-                }
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
             umma_commit(drain);
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t units_done = 0, items_done = 0;
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
     }
 }
 
-// Strip order (padded rank >= 64), described at the top of this file.
+// Strip order (padded rank >= 32), described at the top of this file.
 __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_constant__ DsDbParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -331,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], 2);   // both issuers' commits
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&accS_full[b], 1);
@@ -339,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
         }
         mbar_init(accB_full, 1);
         mbar_init(accB_empty, 128);
-        mbar_init(drain, 1);
+        mbar_init(drain, 2);
         abort_flag = 0;
         fence_barrier_init();
     }
@@ -393,8 +406,10 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
                     mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 6) {
+        // Two issuing threads, as in the tile order: warp 1 the dS MMAs, warp 6 the dB^T MMAs.
         if (lane == 0) {
+            const bool ds_role = warp == 1;
             int s = 0;
             uint32_t ph = 0;
             uint32_t visits = 0, segs = 0, used = 0;
@@ -423,53 +438,58 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
                 const bool visit_first = (u == u0) || it.j == 0;
                 const bool visit_last = (u == u1 - 1) || it.j == it.w - 1;
                 const bool seg_last = (u == u1 - 1) || it.segment_ends(p.rt);
-                if (new_seg) {
+                const uint32_t bs = visits & 1u;
+                if (ds_role) {
+                    if (visit_first) {
+                        if (!mbar_wait(&accS_empty[bs], ((visits >> 1) & 1u) ^ 1u, w, 3)) break;
+                        tc_fence_after();
+                    }
+                } else if (new_seg) {
                     // the previous segment's dB^T accumulators have been flushed
                     if (!mbar_wait(accB_empty, (segs & 1u) ^ 1u, w, 2)) break;
                     tc_fence_after();
                     used = 0;
                 }
-                const uint32_t bs = visits & 1u;
-                if (visit_first) {
-                    if (!mbar_wait(&accS_empty[bs], ((visits >> 1) & 1u) ^ 1u, w, 3)) break;
-                    tc_fence_after();
-                }
                 if (!mbar_wait(&full[s], ph, w, 4)) break;
                 tc_fence_after();
                 const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
-                // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
-                const uint32_t dS_acc = tS + bs * static_cast<uint32_t>(rpad_max);
+                if (ds_role) {
+                    // dS (+)= dY_tile (128 x 128, K = n) * B_a^T (K = n, N = rpad): box h = ks / 4, 32 B per step
+                    const uint32_t dS_acc = tS + bs * static_cast<uint32_t>(rpad_max);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
-                    umma_bf16(dS_acc, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
-                              (visit_first && ks == 0) ? 0u : 1u);
-                }
-                // dB^T[n-block] (+)= dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens,
-                // N = rpad): 16 tokens per step = 2048 B of dY and 16 * rb B of S'
-                const uint32_t dB_acc = tB + static_cast<uint32_t>(it.j * rpad_max);
-                const bool fresh = ((used >> it.j) & 1u) == 0u;
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint64_t h = static_cast<uint64_t>(ks >> 2), kk = static_cast<uint64_t>(ks & 3);
+                        umma_bf16(dS_acc, ds_a0 + so + h * 1024u + kk * 2u, ds_b0 + so + h * bbox16 + kk * 2u, idesc_s,
+                                  (visit_first && ks == 0) ? 0u : 1u);
+                    }
+                    umma_commit(&empty[s]);
+                    if (visit_last) {
+                        umma_commit(&accS_full[bs]);
+                        ++visits;
+                    }
+                } else {
+                    // dB^T[n-block] (+)= dY_tile^T (M = n: two 64-wide atoms, K = tokens) * S'_tile (K = tokens,
+                    // N = rpad): 16 tokens per step = 2048 B of dY and 16 * rb B of S'
+                    const uint32_t dB_acc = tB + static_cast<uint32_t>(it.j * rpad_max);
+                    const bool fresh = ((used >> it.j) & 1u) == 0u;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
-                              (fresh && ks == 0) ? 0u : 1u);
-                used |= 1u << it.j;
-                umma_commit(&empty[s]);
-                if (visit_last) {
-                    umma_commit(&accS_full[bs]);
-                    ++visits;
-                }
-                new_seg = seg_last;
-                if (seg_last) {
-                    umma_commit(accB_full);
-                    ++segs;
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
+                                  (fresh && ks == 0) ? 0u : 1u);
+                    used |= 1u << it.j;
+                    umma_commit(&empty[s]);
+                    new_seg = seg_last;
+                    if (seg_last) {
+                        umma_commit(accB_full);
+                        ++segs;
+                    }
                 }
                 if (++s == S) { s = 0; ph ^= 1u; }
             }
             umma_commit(drain);
             mbar_wait_drain(drain, 0, p.ctl.wait_ns);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         const int quad = warp & 3;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t visits = 0, segs = 0, used = 0;
