@@ -600,7 +600,9 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
             p.off_bits = p.stage_bytes;
             p.stage_bytes += 2048;
         }
-        p.stages = mask_ring_stages(p.stage_bytes, 8);
+        // three mask groups where the ring holds three stages (as the down-projection), else two
+        p.groups = mask_ring_stages(p.stage_bytes, 8, 3) >= 3 ? 3 : 2;
+        p.stages = mask_ring_stages(p.stage_bytes, 8, p.groups);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
         // plain launches on both sides of the event waits: a programmatic launch could start before the
         // other stream's work it waits for is done
@@ -650,7 +652,8 @@ lora_status run_dora_norm(const Call& c, const DoraFwd& d, const uint16_t* W, co
     for (int a = 1; a <= kMaxAdapters; ++a) pu.unit_begin[a] = pu.units;
     pu.off_d = 32768;
     pu.stage_bytes = pu.off_d + 256 * static_cast<uint32_t>(rp);
-    pu.stages = mask_ring_stages(pu.stage_bytes, 8);
+    pu.groups = mask_ring_stages(pu.stage_bytes, 8, 3) >= 3 ? 3 : 2;
+    pu.stages = mask_ring_stages(pu.stage_bytes, 8, pu.groups);
     const int grid = static_cast<int>(std::min<int64_t>(pu.units, c.sms));
     LORA_CUDA(timed(kDoraU, c.stream, [&] { return launch_da(pu, grid, c.stream); }));
     LORA_CUDA(timed(kDoraNorm, c.stream, [&] {

@@ -21,11 +21,9 @@ namespace lora {
 
 namespace {
 
-constexpr int kMaskWarps = 4 * kMaskGroups;        // warps 2.. mask, and run the epilogue
-constexpr int kMaskThreads = 32 * kMaskWarps;
-constexpr int kThreads = 64 + kMaskThreads;        // + warp 0 TMA, warp 1 MMA
+// Warps 2.. mask (and run the epilogue) in G groups of four; warp 0 is the TMA producer, warp 1 the MMA issuer.
 constexpr int kGroupThreads = 128;                // a mask group: four warps, one per TMEM lane quadrant
-constexpr int kGroups = kMaskGroups;               // mask groups, taking stages in turn (S % kGroups == 0)
+constexpr int threads_of(int groups) { return 64 + kGroupThreads * groups; }
 constexpr int kChunks = 16;                        // 16-byte chunks of a token row (two 64-feature boxes)
 constexpr int kBatch = 8;                          // Philox calls computed before their chunks are masked
 static_assert(kGroupThreads == 128, "a group is four warps: one thread per token row, one warp per TMEM lane quadrant");
@@ -66,7 +64,10 @@ __device__ __forceinline__ void da_next(DaUnit& d, const DaParams& p) {
     d.tile = p.rt.active_tiles[p.rt.adapter_begin[d.a] + d.ti];
 }
 
-__global__ void __launch_bounds__(kThreads, 1) da_kernel(const __grid_constant__ DaParams p) {
+// G mask groups take the ring's stages in turn (S % G == 0).
+template <int G>
+__global__ void __launch_bounds__(threads_of(G), 1) da_kernel(const __grid_constant__ DaParams p) {
+    constexpr int kGroups = G;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     const int S = p.stages;
@@ -370,14 +371,18 @@ __global__ void stuck_wait_kernel(DevCtl ctl) {
 
 }  // namespace
 
-size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 2 * kGroups + 1) * 8 + 16; }
+size_t da_smem_bytes(const DaParams& p) { return 1024 + p.stages * p.stage_bytes + (3 * p.stages + 2 * p.groups + 1) * 8 + 16; }
 
 cudaError_t da_configure() {
-    return cudaFuncSetAttribute(da_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    cudaError_t e = cudaFuncSetAttribute(da_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(da_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    return e;
 }
 
 cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream, bool pdl) {
-    return launch_k(pdl, da_kernel, dim3(grid), dim3(kThreads), da_smem_bytes(p), stream, p);
+    if (p.groups == 3) return launch_k(pdl, da_kernel<3>, dim3(grid), dim3(threads_of(3)), da_smem_bytes(p), stream, p);
+    if (p.groups == 2) return launch_k(pdl, da_kernel<2>, dim3(grid), dim3(threads_of(2)), da_smem_bytes(p), stream, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream, bool pdl) {

@@ -137,6 +137,7 @@ struct DaParams {
     CUtensorMap mapBits;               // optional: the forward's keep bits {k/8, m} bytes, box {16, 128}, no swizzle
     int32_t use_bits;                  // 1: the stage's keep bits come with X (at off_bits) instead of from Philox
     uint32_t off_bits;
+    int32_t groups;                    // mask groups of four warps (2 or 3); stages % groups == 0
 };
 
 }  // namespace lora
