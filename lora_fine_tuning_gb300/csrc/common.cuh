@@ -543,6 +543,24 @@ __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
 // finishing fp32 accumulators
 // ---------------------------------------------------------------------------
 
+// The per-row routing the finalize kernels look up for every element: the adapter of each tile and each
+// adapter's rank and scale, copied once per CTA from the kernel's parameters into shared memory (a lookup
+// with a per-thread index in parameter space is far slower than one in shared memory).
+struct RowRouting {
+    int8_t owner[kMaxTiles];
+    int32_t rank[kMaxAdapters];
+    float scale[kMaxAdapters];
+};
+
+__device__ __forceinline__ void load_row_routing(RowRouting& s, const Routing& rt) {
+    for (int i = threadIdx.x; i < rt.n_tiles; i += blockDim.x) s.owner[i] = rt.tile_adapter[i];
+    if (threadIdx.x < kMaxAdapters) {
+        s.rank[threadIdx.x] = rt.ad[threadIdx.x].rank;
+        s.scale[threadIdx.x] = rt.ad[threadIdx.x].scale;
+    }
+    __syncthreads();
+}
+
 // Four fp32 accumulators read from L2 (written there by reductions).
 __device__ __forceinline__ float4 ld_l2_f4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 

@@ -328,6 +328,8 @@ __global__ void __launch_bounds__(threads_of(G), 1) da_kernel(const __grid_const
 // dA_a = bf16(acc_a) (k x r_a), accumulators cleared; dSq rows of active tiles cleared.
 __global__ void __launch_bounds__(256, 4) finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
                                    int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap) {
+    __shared__ RowRouting sr;
+    load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
     pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(256, 4) finalize_da_kernel(float* __restrict__
     const uint32_t total = static_cast<uint32_t>(m) * g8;
     for (uint32_t i = static_cast<uint32_t>(tid); i < total; i += static_cast<uint32_t>(stride)) {
         const uint32_t t = i / g8;
-        if (rt.tile_adapter[t >> 7] < 0) continue;
+        if (sr.owner[t >> 7] < 0) continue;
         stg128(dsq + static_cast<int64_t>(t) * ld + (i - t * g8) * 8, make_uint4(0u, 0u, 0u, 0u));
     }
 }

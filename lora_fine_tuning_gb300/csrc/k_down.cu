@@ -327,6 +327,8 @@ __global__ void __launch_bounds__(threads_of(G), 1) down_proj_kernel(const __gri
 // r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.
 __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
                                   const __grid_constant__ Routing rt) {
+    __shared__ RowRouting sr;
+    load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
     pdl_trigger();
     // m * ld / 8 stays below 2^31: 32-bit index arithmetic
@@ -335,10 +337,10 @@ __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ 
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
         const uint32_t t = i / g8;
         const int c0 = static_cast<int>(i - t * g8) * 8;
-        const int a = rt.tile_adapter[t >> 7];
+        const int a = sr.owner[t >> 7];
         if (a < 0) continue;
         finish_row(acc + static_cast<int64_t>(t) * ld + c0, out + static_cast<int64_t>(t) * ld + c0,
-                   rt.ad[a].rank - c0, 8, rt.ad[a].scale);
+                   sr.rank[a] - c0, 8, sr.scale[a]);
     }
 }
 

@@ -567,6 +567,8 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
 __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
                                      float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
                                      const __grid_constant__ AdapterPtrs dbp, int32_t parts) {
+    __shared__ RowRouting sr;
+    load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
     pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -578,9 +580,9 @@ __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict
         for (uint32_t i = static_cast<uint32_t>(tid); i < total_s; i += static_cast<uint32_t>(stride)) {
             const uint32_t t = i / g8;
             const int c0 = static_cast<int>(i - t * g8) * 8;
-            const int a = rt.tile_adapter[t >> 7];
+            const int a = sr.owner[t >> 7];
             if (a < 0) continue;
-            const int valid = rt.ad[a].rank;
+            const int valid = sr.rank[a];
             float v[8];
             if (c0 < valid) {
                 float* src = dS_acc + static_cast<int64_t>(t) * ld + c0;
@@ -591,7 +593,7 @@ __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict
                 st_zero_f4(src + 4);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * rt.ad[a].scale : 0.f;
+            for (int e = 0; e < 8; ++e) v[e] = (c0 + e < valid) ? v[e] * sr.scale[a] : 0.f;
             uint4 pk;
             pk.x = pack_bf16x2(v[0], v[1]);
             pk.y = pack_bf16x2(v[2], v[3]);

@@ -65,6 +65,27 @@ def test_single_shapes(m, k, n, r, alpha, p, seed):
     check_single_full(raw, out, alpha, p, seed)
 
 
+# Shapes whose GEMMs leave CTA pairs idle: fewer tiles than pairs, and three full waves plus a partial one,
+# at larger k and n than the other cases (the square 4096 sweep's small-m points), with rank-r tails.
+@pytest.mark.parametrize("m,k,n,r,alpha,p,seed", [
+    (1024, 4096, 4096, 16, 2.0, 0.1, 61),     # 64 tiles in each GEMM
+    (768, 2048, 3072, 64, 1.0, 0.2, 62),      # 36 forward tiles, 24 backward tiles
+    (4096, 4096, 4096, 32, 2.0, 0.1, 63),     # 256 tiles: three full waves, the fourth 28 tiles
+])
+def test_partial_wave_shapes(m, k, n, r, alpha, p, seed):
+    raw, out = run_single(m, k, n, r, alpha, p, seed)
+    check_single_full(raw, out, alpha, p, seed)
+
+
+def test_partial_wave_multi_adapter():
+    """Four adapters on a 1024-row packed batch at k = n = 4096: fewer GEMM tiles than CTA pairs, and tiles
+    whose two 128-row halves carry different adapters' tails."""
+    k, n, seed = 4096, 4096, 64
+    batch, segments, raw = multi_case(k, n, 1024, MULTI_SPECS, seed)
+    adapters, Y, S, mask, dX = run_multi(k, n, segments, raw, MULTI_SPECS, seed)
+    check_multi(k, n, segments, raw, MULTI_SPECS, seed, adapters, Y, S, mask, dX)
+
+
 def test_no_dropout_is_merged_weight():
     """p = 0: Y = X (W + alpha A B), masks all ones."""
     m, k, n, r, alpha = 256, 256, 512, 16, 2.0
