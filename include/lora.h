@@ -108,8 +108,34 @@ typedef struct {
 } lora_segment;
 
 /* Workspace bytes sufficient for every call below with these sizes
- * (r_max: the largest rank; n_adapters: adapters per call, >= 1). */
+ * (r_max: the largest rank; n_adapters: adapters per call, >= 1), in the
+ * current reduction mode (lora_set_deterministic): the deterministic mode
+ * needs a larger workspace, sized for the current device. */
 size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters);
+
+/* Reduction mode of every later call in this process (0 by default).
+ *
+ * The rank-r passes split their sums over many CTAs: S over the features
+ * of each token tile, dS over n, dA over the tokens of each adapter, dB over
+ * the tokens.  In the default mode (0) each CTA adds its partial into an fp32
+ * accumulator with hardware reductions, whose order varies from call to
+ * call, so the low bits of S_saved, dX, dA and dB may differ between two
+ * calls on the same inputs (the keep mask and the routing never do).
+ *
+ * Mode 1 makes every output of lora_fwd, lora_bwd, multi_lora_fwd and
+ * multi_lora_bwd bit-identical from call to call on the same device and
+ * sizes (the LoRAFusion notes, papers.chlience.com, list the seed and the
+ * mixed precision among the things a run should be able to re-check): each
+ * CTA writes its partial of S, dS and dA to a slot of its own in the
+ * workspace and the finalize passes add an item's slots in CTA order; dB is
+ * computed in a second read of dY in which every dB element is the sum of at
+ * most two partials onto zero (fp32 addition of two terms commutes exactly).
+ * Cost: the second read of dY and a larger workspace.  Set the mode before
+ * sizing workspaces and between calls; a call sizes its work by the mode it
+ * finds.  DoRA's norm and dmag reductions stay atomic in both modes.
+ * LORA_EINVAL unless `on` is 0 or 1. */
+lora_status lora_set_deterministic(int32_t on);
+int32_t lora_get_deterministic(void);
 
 /* Forward, one adapter.  Writes Y (m x n), S_saved (m x r: alpha * S in bf16,
  * opaque state for lora_bwd) and, if mask_bits is not NULL (16-byte

@@ -38,6 +38,15 @@ def lora_workspace_size(m: int, k: int, n: int, r_max: int, n_adapters: int = 1)
     return int(native.lib().lora_workspace_size(m, k, n, r_max, n_adapters))
 
 
+def lora_set_deterministic(on: bool) -> None:
+    """Bit-reproducible reductions for every later call (see include/lora.h); sizes workspaces anew."""
+    native.check("lora_set_deterministic", native.lib().lora_set_deterministic(1 if on else 0))
+
+
+def lora_get_deterministic() -> bool:
+    return bool(native.lib().lora_get_deterministic())
+
+
 def workspace(m: int, k: int, n: int, r_max: int, n_adapters: int = 1, device=None) -> torch.Tensor:
     """A cached, zero-initialised workspace large enough for these sizes."""
     device = torch.device(device or torch.cuda.current_device())

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -266,10 +267,25 @@ struct Layout {
     size_t dsq = 0;         // m x s_ld bf16
     size_t acc = 0;         // per-adapter dB^T (n x rpad) and dA (k x rpad) fp32
     size_t acc_floats = 0;
+    size_t slots = 0;       // deterministic mode only: partial sums of split items (cleared by their finalize)
     size_t total = 0;
 };
 
-Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int nad) {
+// Deterministic mode: bytes of the slot region, whose slots (128 rows each) hold the partial sums of output
+// items split over CTAs (plan.h, Slots): S' and dS items are active tiles (s_ld floats a row), dA items are
+// (adapter, 128-feature block) pairs (rpad_max floats a row).  `ctas` bounds the grid of every such pass.
+size_t det_slot_bytes(int64_t m, int64_t k, int s_ld, int rpad_max, int nad, int ctas) {
+    const int64_t n_tiles = (m + kTileM - 1) / kTileM;
+    const int64_t nfb = (k + 127) / 128;
+    const size_t s = static_cast<size_t>(n_tiles + ctas) * 128 * s_ld * 4;
+    const size_t d = static_cast<size_t>(std::max(nad, 1) * nfb + ctas) * 128 * rpad_max * 4;
+    return std::max(s, d);
+}
+
+// Deterministic mode (lora_set_deterministic): split sums go through the slot region in a fixed order.
+std::atomic<int> g_deterministic{0};
+
+Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int nad, int det_ctas = 0) {
     Layout L;
     size_t off = 0;
     L.status = off;
@@ -283,6 +299,12 @@ Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int n
     for (int a = 0; a < nad; ++a) floats += static_cast<size_t>(n + k) * rpads[a];
     L.acc_floats = floats;
     off = up(off + floats * 4);
+    if (det_ctas > 0) {
+        int rpad_max = 16;
+        for (int a = 0; a < nad; ++a) rpad_max = std::max(rpad_max, rpads[a]);
+        L.slots = off;
+        off = up(off + det_slot_bytes(m, k, std::max(s_ld, 8), rpad_max, nad, det_ctas));
+    }
     L.total = off;
     return L;
 }
@@ -298,6 +320,7 @@ struct Call {
     Layout L;
     uint8_t* ws = nullptr;
     int sms = 0;
+    bool det = false;    // deterministic mode for this call
     cudaStream_t stream = nullptr;
 };
 
@@ -342,8 +365,15 @@ lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_se
         if (a >= 0) c.rt.active_tiles[c.rt.adapter_begin[a] + fill[a]++] = static_cast<uint16_t>(t);
     }
     c.rt.n_active = c.rt.adapter_begin[nad > 0 ? nad : 0];
-    // workspace
-    c.L = layout(m, k, n, s_ld, c.rpads, nad);
+    // workspace (the deterministic mode's slot region is sized by the device's grid: device set-up first)
+    c.det = g_deterministic.load() != 0;
+    int det_ctas = 0;
+    if (c.det) {
+        st = device_setup(&c.sms);
+        if (st) return st;
+        det_ctas = 2 * c.sms;
+    }
+    c.L = layout(m, k, n, s_ld, c.rpads, nad, det_ctas);
     int64_t off = 0;
     for (int a = 0; a < nad; ++a) {
         c.rt.ad[a].dB_off = off;
@@ -416,6 +446,7 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         p.groups = mask_ring_stages(p.stage_bytes, 8, 3) >= 3 ? 3 : 2;
         p.stages = mask_ring_stages(p.stage_bytes, 8, p.groups);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        if (c.det) p.sl = Slots{reinterpret_cast<float*>(c.ws + c.L.slots), p.units, grid, c.s_ld};
         LORA_CUDA(timed(kDownProj, c.stream, [&] { return launch_down(p, grid, c.stream); }));
         LORA_CUDA(timed(kFinalizeS, c.stream, [&] { return launch_finalize_s(p, c.sms, c.stream); }));
     }
@@ -518,10 +549,29 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         // the Llama-3.1-8B up-proj 52 tile / 61 strip; rank 32 on the square 4096 layer at m = 16384
         // 52.3 tile / 46.5 strip, at m = 4096 21.9 tile / 23.7 strip.
         p.strip = rpm >= kStripMinRank ? std::max(1, std::min<int>(p.nnb, (two_per_sm ? 256 : 512) / static_cast<int>(rpm) - 2)) : 0;
+        p.parts = kPartDs | kPartDb;
         const int64_t ctas = static_cast<int64_t>(two_per_sm ? 2 : 1) * c.sms;
-        const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
-        LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
-        LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs | kPartDb, c.sms, c.stream); }));
+        if (!c.det) {
+            const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
+            LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
+            LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs | kPartDb, c.sms, c.stream); }));
+        } else {
+            // Deterministic mode, two reads of dY.  dS: tile order, each CTA's partial of a tile in its own slot,
+            // added in CTA order by finalize_bwd1.  dB: strips of one n-block, each split between at most two CTAs,
+            // so every dB^T element is the sum of at most two reductions onto zero, which commute exactly.
+            p.strip = 0;
+            p.parts = kPartDs;
+            const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
+            p.sl = Slots{reinterpret_cast<float*>(c.ws + c.L.slots), p.units, grid, c.s_ld};
+            LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
+            LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs, c.sms, c.stream); }));
+            p.strip = 1;
+            p.parts = kPartDb;
+            p.sl = Slots{};
+            const int grid_db = p.nnb * (c.rt.n_active >= 2 ? 2 : 1);
+            LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid_db, c.stream); }));
+            LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDb, c.sms, c.stream); }));
+        }
     }
 
     // dA only needs dSq (written above) and X, not dX: it is forked onto the side stream, launched after
@@ -604,6 +654,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.groups = mask_ring_stages(p.stage_bytes, 8, 3) >= 3 ? 3 : 2;
         p.stages = mask_ring_stages(p.stage_bytes, 8, p.groups);
         const int grid = static_cast<int>(std::min<int64_t>(p.units, c.sms));
+        if (c.det) p.sl = Slots{reinterpret_cast<float*>(c.ws + c.L.slots), p.units, grid, static_cast<int32_t>(rpm)};
         // plain launches on both sides of the event waits: a programmatic launch could start before the
         // other stream's work it waits for is done
         LORA_CUDA(timed(kDa, side, [&] { return launch_da(p, grid, side, false); }));
@@ -706,8 +757,26 @@ size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32
     int rp[kMaxAdapters];
     const int nad = std::min<int32_t>(std::max<int32_t>(n_adapters, 1), kMaxAdapters);
     for (int a = 0; a < nad; ++a) rp[a] = rank_pad(std::max(r_max, 8));
-    return layout(m, k, n, std::max(r_max, 8), rp, nad).total;
+    int det_ctas = 0;
+    if (g_deterministic.load() != 0) {
+        // the slot region grows with the grid: two CTAs per SM of the current device (1024 if none answers)
+        int dev = 0, sms = 0;
+        det_ctas = (cudaGetDevice(&dev) == cudaSuccess &&
+                    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+                       ? 2 * sms
+                       : 1024;
+        cudaGetLastError();   // a failed query leaves no sticky error behind
+    }
+    return layout(m, k, n, std::max(r_max, 8), rp, nad, det_ctas).total;
 }
+
+lora_status lora_set_deterministic(int32_t on) {
+    if (on != 0 && on != 1) return LORA_EINVAL;
+    g_deterministic.store(on);
+    return LORA_OK;
+}
+
+int32_t lora_get_deterministic(void) { return g_deterministic.load(); }
 
 lora_status multi_lora_fwd(const lora_bf16* X, const lora_bf16* W, const lora_adapter* adapters, int32_t n_adapters,
                            const lora_segment* segments, int32_t n_segments, uint64_t seed, int64_t m, int64_t k,

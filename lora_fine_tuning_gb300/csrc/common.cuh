@@ -548,12 +548,14 @@ __device__ __forceinline__ uint32_t keep_byte(uint4 w, uint32_t T) {
 // with a per-thread index in parameter space is far slower than one in shared memory).
 struct RowRouting {
     int8_t owner[kMaxTiles];
+    int16_t active[kMaxTiles];   // tile -> its index in the active tile list (tiles with an adapter)
     int32_t rank[kMaxAdapters];
     float scale[kMaxAdapters];
 };
 
 __device__ __forceinline__ void load_row_routing(RowRouting& s, const Routing& rt) {
     for (int i = threadIdx.x; i < rt.n_tiles; i += blockDim.x) s.owner[i] = rt.tile_adapter[i];
+    for (int i = threadIdx.x; i < rt.n_active; i += blockDim.x) s.active[rt.active_tiles[i]] = static_cast<int16_t>(i);
     if (threadIdx.x < kMaxAdapters) {
         s.rank[threadIdx.x] = rt.ad[threadIdx.x].rank;
         s.scale[threadIdx.x] = rt.ad[threadIdx.x].scale;
@@ -568,7 +570,38 @@ __device__ __forceinline__ void st_zero_f4(float* p) {
     *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+__device__ __forceinline__ void st_f4(float* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+
+// Row `row` (of 128), columns c0 .. c0 + 7, of item `item` whose units are [b, e): its slots added in CTA
+// order.  Each slot element read is cleared (the producers wrote exactly the elements their finalize reads),
+// so the workspace is zero again after the call, whatever layout the next call puts over these bytes.
+__device__ __forceinline__ void slot_sum8(const Slots& sl, int64_t item, int64_t b, int64_t e, int row, int c0,
+                                          float (&v)[8]) {
+#pragma unroll
+    for (int x = 0; x < 8; ++x) v[x] = 0.f;
+    const int c_lo = slot_cta(b, sl.units, sl.grid), c_hi = slot_cta(e - 1, sl.units, sl.grid);
+    for (int c = c_lo; c <= c_hi; ++c) {
+        float* src = sl.base + ((item + c) * 128 + row) * static_cast<int64_t>(sl.ld) + c0;
+        const float4 x = ld_l2_f4(src);
+        const float4 y = ld_l2_f4(src + 4);
+        st_zero_f4(src);
+        st_zero_f4(src + 4);
+        v[0] += x.x; v[1] += x.y; v[2] += x.z; v[3] += x.w; v[4] += y.x; v[5] += y.y; v[6] += y.z; v[7] += y.w;
+    }
+}
+
 __device__ __forceinline__ uint16_t bf16_bits(float v) { return static_cast<uint16_t>(pack_bf16x2(v, 0.f) & 0xFFFFu); }
+
+// Eight sums -> bf16: out[e] = scale * v[e] for e < valid, 0 for valid <= e < 8.
+__device__ __forceinline__ void store_row8(uint16_t* out, const float (&v)[8], int valid, float scale) {
+    float w[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) w[e] = e < valid ? v[e] * scale : 0.f;
+    stg128(out, make_uint4(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3]), pack_bf16x2(w[4], w[5]),
+                           pack_bf16x2(w[6], w[7])));
+}
 
 // Row of an fp32 accumulator -> bf16 row: out[c] = scale * acc[c] for c < valid,
 // 0 for valid <= c < width; the accumulator row is zeroed.  width % 8 == 0.

@@ -296,17 +296,25 @@ __global__ void __launch_bounds__(threads_of(G), 1) da_kernel(const __grid_const
                 tc_fence_after();
                 const int64_t j = static_cast<int64_t>(d.fb) * 128 + quad * 32 + lane;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * static_cast<uint32_t>(rpad_max);
-                float* dst = p.acc_base + ad.dA_off + j * ad.rpad;
+                // deterministic mode: this CTA's partial of item (adapter, feature block) goes to slot item + CTA
+                const int64_t item = static_cast<int64_t>(d.a) * p.nfb + d.fb;
+                float* dst = p.sl.base ? p.sl.base + ((item + blockIdx.x) * 128 + quad * 32 + lane) * p.sl.ld
+                                       : p.acc_base + ad.dA_off + j * ad.rpad;
                 for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_ld_wait();
                     if (j < p.k) {
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4)
-                            if (c0 + q < ad.rank)
+                        for (int q = 0; q < 16; q += 4) {
+                            if (c0 + q >= ad.rank) continue;
+                            if (p.sl.base)
+                                st_f4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                      __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                            else
                                 red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -327,7 +335,8 @@ __global__ void __launch_bounds__(threads_of(G), 1) da_kernel(const __grid_const
 
 // dA_a = bf16(acc_a) (k x r_a), accumulators cleared; dSq rows of active tiles cleared.
 __global__ void __launch_bounds__(256, 4) finalize_da_kernel(float* __restrict__ acc_base, int64_t k, uint16_t* __restrict__ dsq, int64_t m,
-                                   int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap) {
+                                   int32_t ld, const __grid_constant__ Routing rt, const __grid_constant__ AdapterPtrs dap,
+                                   const Slots sl, int32_t nfb, const __grid_constant__ UnitBegin ub) {
     __shared__ RowRouting sr;
     load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
@@ -343,8 +352,19 @@ __global__ void __launch_bounds__(256, 4) finalize_da_kernel(float* __restrict__
         for (uint32_t i = static_cast<uint32_t>(tid); i < total; i += static_cast<uint32_t>(stride)) {
             const uint32_t j = i / g8;
             const int c0 = static_cast<int>(i - j * g8) * 8;
-            finish_row(acc_base + ad.dA_off + static_cast<int64_t>(j) * ad.rpad + c0,
-                       dap.p[a] + static_cast<int64_t>(j) * ad.rank + c0, 8, 8, 1.0f);
+            if (sl.base == nullptr) {
+                finish_row(acc_base + ad.dA_off + static_cast<int64_t>(j) * ad.rpad + c0,
+                           dap.p[a] + static_cast<int64_t>(j) * ad.rank + c0, 8, 8, 1.0f);
+                continue;
+            }
+            // deterministic mode: the item's slots added in CTA order; its units are the adapter's tiles
+            // of feature block j / 128
+            const int fb = static_cast<int>(j >> 7);
+            const int64_t n_a = rt.adapter_begin[a + 1] - rt.adapter_begin[a];
+            const int64_t b = ub.u[a] + static_cast<int64_t>(fb) * n_a;
+            float v[8];
+            slot_sum8(sl, static_cast<int64_t>(a) * nfb + fb, b, b + n_a, static_cast<int>(j & 127), c0, v);
+            store_row8(dap.p[a] + static_cast<int64_t>(j) * ad.rank + c0, v, 8, 1.0f);
         }
     }
     const uint32_t g8 = static_cast<uint32_t>(ld / 8);
@@ -388,8 +408,10 @@ cudaError_t launch_da(const DaParams& p, int grid, cudaStream_t stream, bool pdl
 }
 
 cudaError_t launch_finalize_da(const DaParams& p, int sms, cudaStream_t stream, bool pdl) {
+    UnitBegin ub;
+    for (int a = 0; a <= kMaxAdapters; ++a) ub.u[a] = p.unit_begin[a];
     return launch_k(pdl, finalize_da_kernel, dim3(2 * sms), dim3(256), 0, stream, p.acc_base, p.k, p.dsq, p.m, p.ld,
-                    p.rt, p.dA);
+                    p.rt, p.dA, p.sl, p.nfb, ub);
 }
 
 cudaError_t launch_stuck_wait(DevCtl ctl, cudaStream_t stream) {

@@ -294,17 +294,26 @@ __global__ void __launch_bounds__(threads_of(G), 1) down_proj_kernel(const __gri
                 const AdapterDev ad = p.rt.ad[a];
                 const int64_t orow = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quad * 32) << 16) + b * static_cast<uint32_t>(rpad_max);
+                // deterministic mode: this CTA's partial of active tile it.slot goes to slot it.slot + CTA
+                float* const out = p.sl.base
+                                       ? p.sl.base + ((static_cast<int64_t>(it.slot) + blockIdx.x) * 128 + quad * 32 + lane) * p.sl.ld
+                                       : p.S_acc + orow * p.ld;
                 for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_ld_wait();
                     if (orow < p.m) {
-                        float* dst = p.S_acc + orow * p.ld + c0;
+                        float* dst = out + c0;
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4)
-                            if (c0 + q < ad.rank)
+                        for (int q = 0; q < 16; q += 4) {
+                            if (c0 + q >= ad.rank) continue;
+                            if (p.sl.base)
+                                st_f4(dst + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
+                                      __uint_as_float(v[q + 3]));
+                            else
                                 red_add_v4(dst + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -324,9 +333,10 @@ __global__ void __launch_bounds__(threads_of(G), 1) down_proj_kernel(const __gri
 }
 
 // S'[t, c] = bf16(alpha_a / (1 - p_a) * S_acc[t, c]) for c < r_a, 0 for
-// r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.
+// r_a <= c < ld, on rows of tiles that have an adapter; S_acc is cleared.  In
+// deterministic mode (sl.base set) the row's slots are added in CTA order instead.
 __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ acc, uint16_t* __restrict__ out, int64_t m, int32_t ld,
-                                  const __grid_constant__ Routing rt) {
+                                  const __grid_constant__ Routing rt, const Slots sl, int32_t nkb) {
     __shared__ RowRouting sr;
     load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
@@ -339,8 +349,17 @@ __global__ void __launch_bounds__(256, 4) finalize_s_kernel(float* __restrict__ 
         const int c0 = static_cast<int>(i - t * g8) * 8;
         const int a = sr.owner[t >> 7];
         if (a < 0) continue;
-        finish_row(acc + static_cast<int64_t>(t) * ld + c0, out + static_cast<int64_t>(t) * ld + c0,
-                   sr.rank[a] - c0, 8, sr.scale[a]);
+        if (sl.base == nullptr) {
+            finish_row(acc + static_cast<int64_t>(t) * ld + c0, out + static_cast<int64_t>(t) * ld + c0,
+                       sr.rank[a] - c0, 8, sr.scale[a]);
+            continue;
+        }
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+        const int64_t item = sr.active[t >> 7];
+        if (c0 < sr.rank[a]) slot_sum8(sl, item, item * nkb, (item + 1) * nkb, static_cast<int>(t & 127), c0, v);
+        store_row8(out + static_cast<int64_t>(t) * ld + c0, v, sr.rank[a] - c0, sr.scale[a]);
     }
 }
 
@@ -365,7 +384,8 @@ cudaError_t launch_down(const DownParams& p, int grid, cudaStream_t stream) {
 }
 
 cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream) {
-    return launch_pdl(finalize_s_kernel, dim3(2 * sms), dim3(256), 0, stream, p.S_acc, p.S_out, p.m, p.ld, p.rt);
+    return launch_pdl(finalize_s_kernel, dim3(2 * sms), dim3(256), 0, stream, p.S_acc, p.S_out, p.m, p.ld, p.rt, p.sl,
+                      p.nkb);
 }
 
 }  // namespace lora

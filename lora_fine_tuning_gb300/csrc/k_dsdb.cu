@@ -265,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
             bool ok = mbar_wait(&accB_full[bb], (units_done >> 1) & 1u, w, 5);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after();
-            {
+            if (p.parts & kPartDb) {
                 const int64_t nidx = static_cast<int64_t>(nb) * 128 + quad * 32 + lane;
                 float* dst = p.acc_base + ad.dB_off + nidx * ad.rpad;
                 const uint32_t taddr = tB + lane_off + bb * static_cast<uint32_t>(rpad_max);
@@ -281,26 +281,34 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_tile_kernel(const __grid_con
                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&accB_empty[bb]);
             }
+            tc_fence_before();
+            mbar_arrive(&accB_empty[bb]);
             ++units_done;
             if (last) {
                 ok = mbar_wait(accS_full, items_done & 1u, w, 6);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
                 const int64_t row = static_cast<int64_t>(tile) * kTileM + quad * 32 + lane;
-                float* dst = p.dS_acc + row * p.ld;
-                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                // deterministic mode: this CTA's partial of active tile it.slot goes to slot it.slot + CTA
+                float* dst = p.sl.base ? p.sl.base + ((static_cast<int64_t>(it.slot) + blockIdx.x) * 128 + quad * 32 + lane) *
+                                                         p.sl.ld
+                                       : p.dS_acc + row * p.ld;
+                for (int c0 = 0; (p.parts & kPartDs) && c0 < ad.rpad; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(tS + lane_off + c0, v);
                     tmem_ld_wait();
                     if (row < p.m) {
 #pragma unroll
-                        for (int q = 0; q < 16; q += 4)
-                            if (c0 + q < ad.rank)
+                        for (int q = 0; q < 16; q += 4) {
+                            if (c0 + q >= ad.rank) continue;
+                            if (p.sl.base)
+                                st_f4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                      __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                            else
                                 red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
                                            __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -507,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
                 const int64_t row = static_cast<int64_t>(it.tile) * kTileM + quad * 32 + lane;
                 float* dst = p.dS_acc + row * p.ld;
                 const uint32_t taddr = tS + lane_off + bs * static_cast<uint32_t>(rpad_max);
-                for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                for (int c0 = 0; (p.parts & kPartDs) && c0 < ad.rpad; c0 += 16) {
                     uint32_t v[16];
                     tmem_ld16(taddr + c0, v);
                     tmem_ld_wait();
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
                 const bool ok = mbar_wait(accB_full, segs & 1u, w, 6);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
                 tc_fence_after();
-                for (int jj = 0; jj < it.w; ++jj) {
+                for (int jj = 0; (p.parts & kPartDb) && jj < it.w; ++jj) {
                     if (!((used >> jj) & 1u)) continue;
                     const int64_t nidx = static_cast<int64_t>(it.s * J + jj) * 128 + quad * 32 + lane;
                     float* dst = p.acc_base + ad.dB_off + nidx * ad.rpad;
@@ -566,7 +574,8 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
 // (parts & kPartDb).  Every accumulator read is cleared.
 __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict__ dS_acc, uint16_t* __restrict__ dSq, int64_t m, int32_t ld,
                                      float* __restrict__ acc_base, int64_t n, const __grid_constant__ Routing rt,
-                                     const __grid_constant__ AdapterPtrs dbp, int32_t parts) {
+                                     const __grid_constant__ AdapterPtrs dbp, int32_t parts, const Slots sl,
+                                     int32_t nnb) {
     __shared__ RowRouting sr;
     load_row_routing(sr, rt);   // parameters only: before the wait on the previous kernel
     pdl_wait();
@@ -583,6 +592,16 @@ __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict
             const int a = sr.owner[t >> 7];
             if (a < 0) continue;
             const int valid = sr.rank[a];
+            if (sl.base != nullptr) {
+                // deterministic mode: the tile's slots added in CTA order
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = 0.f;
+                const int64_t item = sr.active[t >> 7];
+                if (c0 < valid) slot_sum8(sl, item, item * nnb, (item + 1) * nnb, static_cast<int>(t & 127), c0, v);
+                store_row8(dSq + static_cast<int64_t>(t) * ld + c0, v, valid - c0, sr.scale[a]);
+                continue;
+            }
             float v[8];
             if (c0 < valid) {
                 float* src = dS_acc + static_cast<int64_t>(t) * ld + c0;
@@ -663,7 +682,7 @@ cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
 cudaError_t launch_finalize_bwd1(const DsDbParams& p, int parts, int sms, cudaStream_t stream, bool pdl) {
     if (parts < kPartDs || parts > (kPartDs | kPartDb)) return cudaErrorInvalidValue;
     return launch_k(pdl, finalize_bwd1_kernel, dim3(2 * sms), dim3(256), 0, stream, p.dS_acc, p.dSq, p.m, p.ld,
-                    p.acc_base, p.n, p.rt, p.dB, static_cast<int32_t>(parts));
+                    p.acc_base, p.n, p.rt, p.dB, static_cast<int32_t>(parts), p.sl, p.nnb);
 }
 
 }  // namespace lora

@@ -49,6 +49,26 @@ struct DevCtl {
     uint64_t wait_ns;   // bounded-wait limit
 };
 
+// Fixed-order sums of stream-K partials (the library's deterministic mode).
+// A pass splits its U units into G contiguous CTA ranges [U c / G, U (c+1) / G)
+// with G <= U, so no range is empty.  An output item whose units are [b, e) is
+// then summed by the CTAs slot_cta(b) .. slot_cta(e - 1), and CTA c writes its
+// partial of item i, 128 rows of `ld` floats, to slot i + c: an item starts in
+// the CTA where the one before it ends or later, so slots never collide, and
+// the finalize kernel adds an item's slots in CTA order, the same order on every
+// call, clearing them as it reads.  At most n_items + G - 1 slots are written.
+struct Slots {
+    float* base;     // null: partials are added into the accumulator with fp32 reductions
+    int64_t units;   // U
+    int32_t grid;    // G
+    int32_t ld;      // floats per slot row
+};
+
+// The CTA whose range holds unit u: the largest c with floor(U c / G) <= u.
+__host__ __device__ __forceinline__ int slot_cta(int64_t u, int64_t U, int32_t G) {
+    return static_cast<int>(((u + 1) * G - 1) / U);
+}
+
 // Down-projection: S_acc[t, c] += sum_j (X .* D)[t, j] A_a[j, c] over stream-K
 // ranges of (active tile, 128-wide k-block) units.
 struct DownParams {
@@ -67,6 +87,7 @@ struct DownParams {
     int32_t stages;
     uint32_t stage_bytes;              // X tile (two 16 KB boxes) + 128 rows of A (256 * rpad_max bytes)
     int32_t groups;                    // mask groups of four warps (2 or 4); stages % groups == 0
+    Slots sl;                          // deterministic mode: S partials per (active tile, CTA) slot
 };
 
 // CTA-pair GEMM with the rank-r tail (k_gemm2.cu).
@@ -115,6 +136,13 @@ struct DsDbParams {
     int64_t units;                     // n_active * nnb
     int32_t stages;
     uint32_t stage_bytes, off_b, off_s; // stage layout
+    int32_t parts;                     // kPartDs: flush dS; kPartDb: flush dB^T (the other product is computed, not kept)
+    Slots sl;                          // deterministic mode (tile order): dS partials per (active tile, CTA) slot
+};
+
+// First unit of each adapter in the dA pass's order (the last entry: the unit count).
+struct UnitBegin {
+    int64_t u[kMaxAdapters + 1];
 };
 
 // dA = (X .* D)^T dSq per adapter: per (adapter, 128-feature block, tile) unit.
@@ -138,6 +166,7 @@ struct DaParams {
     int32_t use_bits;                  // 1: the stage's keep bits come with X (at off_bits) instead of from Philox
     uint32_t off_bits;
     int32_t groups;                    // mask groups of four warps (2 or 3); stages % groups == 0
+    Slots sl;                          // deterministic mode: dA partials per (adapter * nfb + feature block, CTA) slot
 };
 
 }  // namespace lora

@@ -17,7 +17,7 @@ STATUS_NAMES = {0: "LORA_OK", 1: "LORA_EINVAL", 2: "LORA_EALIGN", 3: "LORA_ESHAP
                 5: "LORA_ECUDA", 6: "LORA_EWORKSPACE", 7: "LORA_EDEVICE_TIMEOUT", 8: "LORA_ETABLE"}
 
 # Symbols include/lora.h declares, in declaration order.
-EXPORTED = ["lora_workspace_size", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd",
+EXPORTED = ["lora_workspace_size", "lora_set_deterministic", "lora_get_deterministic", "lora_fwd", "lora_bwd", "multi_lora_fwd", "multi_lora_bwd",
             "dora_workspace_size", "dora_weight_norm2", "dora_fwd", "dora_bwd",
             "lora_fwd_static_scratch", "lora_tile_table",
             "lora_keep_threshold", "lora_pack_greedy", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
                                       ctypes.c_float, ctypes.c_size_t)
         sig = {
             "lora_workspace_size": (sz, [i64, i64, i64, i32, i32]),
+            "lora_set_deterministic": (i32, [i32]),
+            "lora_get_deterministic": (i32, []),
             "lora_fwd": (i32, [vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "lora_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, f32, f32, u64, i64, i64, i64, i32, vp, vp, vp, vp, sz, vp]),
             "multi_lora_fwd": (i32, [vp, vp, ctypes.POINTER(LoraAdapter), i32, ctypes.POINTER(LoraSegment), i32, u64,

@@ -25,7 +25,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "lora.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:lora_status|size_t|void|const char\*)\s+(\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:lora_status|size_t|void|int32_t|const char\*)\s+(\w+)\s*\(", text, flags=re.M)
 
 
 def test_header_and_binding_agree():
@@ -179,3 +179,21 @@ def test_dora_workspace_and_validation(lib):
     st = lib.dora_bwd(256, 256, 256, 256, 256, 256, None, 256, 256, 256, 1.0, 0.1, 0, 128, 64, 64, 16, 256, 256,
                       256, None, 256, 256, 1 << 30, None)
     assert st == 1
+
+
+def test_deterministic_mode_setter_and_workspace(lib):
+    """Mode 1 sizes a larger workspace (slot region; no device here: the 1024-CTA bound); other values are
+    rejected and leave the mode unchanged."""
+    base = lib.lora_workspace_size(8192, 4096, 14336, 16, 1)
+    assert lib.lora_get_deterministic() == 0
+    assert lib.lora_set_deterministic(2) == 1           # LORA_EINVAL
+    assert lib.lora_get_deterministic() == 0
+    assert lib.lora_set_deterministic(1) == 0
+    try:
+        det = lib.lora_workspace_size(8192, 4096, 14336, 16, 1)
+    finally:
+        assert lib.lora_set_deterministic(0) == 0
+    # slots: (64 tiles + 1024 CTAs) x 128 rows x 16 floats, or (32 feature blocks + 1024) x 128 x 16, whichever
+    # is larger, rounded up to 256 bytes
+    assert det - base == (64 + 1024) * 128 * 16 * 4
+    assert lib.lora_workspace_size(8192, 4096, 14336, 16, 1) == base
