@@ -36,9 +36,12 @@ import numpy as np  # noqa: E402
 from lora_fine_tuning_gb300 import synth  # noqa: E402
 
 METRIC = "LoRA linear fwd+bwd tokens/s on 1 GB300; % of layer roofline"
-# Kernels the library runs on its side stream, concurrently with the dX GEMM: their event pair spans from
-# the fork (the GEMM's start) to their own end, so their time is not a device duration of their own.
-SIDE_STREAM_KINDS = {"da"}
+# Kernels the library runs on its side stream, concurrently with the dX GEMM, when the backward reads the
+# forward's keep bits (--saved-mask): their event pair spans from the fork (the GEMM's start) to their own
+# end, so their time is not a device duration of their own.  When the backward regenerates the mask (the
+# default; every workload here has k % 128 == 0) the dX GEMM hands its bits to dA, which runs after it on
+# the caller's stream.
+SIDE_STREAM_KINDS_SAVED_MASK = {"da"}
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GB300 datasheet figures (dense bf16, HBM3e), for the fractions of the hardware bound beside the
@@ -264,6 +267,28 @@ class Workload:
             if self.name != GREEDY or j == 0:   # a packed global batch: the tails of all its rows, once
                 F += sum(2 * self.rows_of(i) * r * out for i, (r, _, _) in enumerate(q.specs))
         return F
+
+    def rank_bytes_per_step(self, kind: str, saved_mask: bool = False, deterministic: bool = False):
+        """Algorithmic HBM bytes of one step's launches of a rank-r pass, over the rows they run (bf16 tensors;
+        keep bits one bit an element): down_proj reads X and A_i and writes S' (and the keep bits when the
+        forward keeps them); ds_db reads dY, S' and B_i (dY twice in the deterministic mode); da reads X, the
+        keep bits (handed over by the dX GEMM, or the forward's) and dSq, and writes dA_i."""
+        if kind not in ("down_proj", "ds_db", "da"):
+            return None
+        B = 0
+        for q in (self.parts[:1] if self.name == GREEDY else self.parts):
+            rows_i = [self.rows_of(i) for i in range(len(q.specs))]
+            rows = sum(rows_i)
+            ranks = [r for r, _, _ in q.specs]
+            if kind == "down_proj":
+                B += 2 * rows * q.k + sum(2 * q.k * r + 2 * t * r for t, r in zip(rows_i, ranks))
+                B += rows * q.k // 8 if saved_mask else 0
+            elif kind == "ds_db":
+                B += 2 * rows * q.n * (2 if deterministic else 1)
+                B += sum(2 * t * r + 2 * r * q.n for t, r in zip(rows_i, ranks))
+            else:
+                B += 2 * rows * q.k + rows * q.k // 8 + sum(2 * t * r + 2 * q.k * r for t, r in zip(rows_i, ranks))
+        return B
 
     def resident_bytes(self) -> int:
         """Bytes of X, W, dY, Y and dX over all linears: what one step streams through L2."""
@@ -773,6 +798,8 @@ def run_native(args):
     dev = torch.device("cuda", local)
     wl = Workload(args.workload, args.m, args.r, packer=native.pack_microbatches)
     stream = torch.cuda.current_stream(dev)
+    from lora_fine_tuning_gb300 import api
+    api.lora_set_deterministic(args.deterministic)   # before any workspace is sized
     prob = DeviceProblem(wl, dev, stream, args.saved_mask)
 
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -886,13 +913,14 @@ def run_native(args):
         return
 
     peaks, peak_kind = load_peaks()
+    side_kinds = SIDE_STREAM_KINDS_SAVED_MASK if args.saved_mask else set()
     # the instrumented window's length decides which measured peak applies: the burst figure for a
     # short window, the seconds-long (power-capped) figure for a long one
     long_window = instrumented_ms / 1e3 >= SUSTAINED_SECONDS
     tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) if long_window else peaks["bf16_tflops"]
     # dominant kernel: the largest summed device time among the kernels on the launch stream
     dom_name, (dom_ms, dom_launches) = max(((kn, tc) for kn, tc in kernel_times.items()
-                                            if kn not in SIDE_STREAM_KINDS), key=lambda kv: kv[1][0])
+                                            if kn not in side_kinds), key=lambda kv: kv[1][0])
     dom_flops = wl.gemm_flops_per_step(dom_name)
     if dom_flops is not None:
         # FLOPs of all its launches over their summed device time (one launch per step for one linear)
@@ -926,12 +954,17 @@ def run_native(args):
 
     kernels = {}
     for kname, (t, cnt) in sorted(kernel_times.items(), key=lambda kv: -kv[1][0]):
-        if kname in SIDE_STREAM_KINDS:
+        if kname in side_kinds:
             kernels[kname] = {"ms_fork_to_end": t / max(1, cnt), "launches": cnt,
                               "stream": "side stream, concurrent with gemm_bwd"}
         else:
             kernels[kname] = {"ms_per_launch": t / max(1, cnt), "launches": cnt,
                               "share": t / max(1e-9, instrumented_ms)}
+            nbytes = wl.rank_bytes_per_step(kname, args.saved_mask, args.deterministic)
+            if nbytes is not None and t > 0:
+                gbs = nbytes * args.steps / (t / 1e3) / 1e9
+                kernels[kname].update({"algorithmic_bytes_per_step": nbytes, "achieved_gbs": gbs,
+                                       "frac_of_hbm": gbs / peaks["hbm_gbs"]})
     gpu_launches = sum(cnt for kname, (t, cnt) in kernel_times.items() if kname != "memset")
 
     cpu = None
@@ -942,7 +975,9 @@ def run_native(args):
               "r": [[r for r, _, _ in q.specs] for q in wl.parts], "tokens_per_step": wl.tokens,
               "parallelism": f"replicas x{ws_n}" if ws_n > 1 else "single GPU", "l2": l2_note,
               "saved_for_backward": ("S_saved and the keep bits (m x k/8 bytes) written by the forward"
-                                     if args.saved_mask else "S_saved; the backward regenerates the keep mask from the seed")}
+                                     if args.saved_mask else "S_saved; the backward regenerates the keep mask from the seed"),
+              "reductions": ("deterministic: fixed-order sums of per-CTA partials, dY read twice" if args.deterministic
+                             else "fp32 atomic reductions of per-CTA partials")}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws_n, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, Llama-shaped)", "config": config,
@@ -982,6 +1017,8 @@ def main():
                     help="minimum length of the sustained leg's timed window")
     ap.add_argument("--saved-mask", action="store_true",
                     help="the forward writes the keep bits and the backward reads them (default: regenerated)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="bit-reproducible reductions (lora_set_deterministic(1)): fixed-order sums, a second dY read")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

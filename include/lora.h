@@ -51,10 +51,13 @@
  *    lock while it enqueues work.  Calls on different streams with different
  *    workspaces are independent on the GPU too: the backward's side stream
  *    (below) belongs to the caller's stream.
- *  - The backward forks its dA pass onto a side stream and joins it back to
- *    `stream` before it returns work to it.  The first backward call on a
- *    stream creates that stream's side stream and two events; make it before
- *    any stream capture.
+ *  - When the backward regenerates the keep mask (no mask_bits given) and
+ *    k % 128 == 0, the dX GEMM writes the decisions it regenerates for its
+ *    own epilogue into the workspace and the dA pass reads them after it.
+ *    Otherwise the backward forks its dA pass onto a side stream, beside the
+ *    dX GEMM, and joins it back to `stream` before it returns work to it; the
+ *    first such call on a stream creates that stream's side stream and two
+ *    events: make it before any stream capture.
  */
 #ifndef LORA_GB300_H
 #define LORA_GB300_H
@@ -306,8 +309,9 @@ const char* lora_status_string(lora_status s);
  * time in ms and the number of launches.  Kinds: 0 down-projection,
  * 1 finalize S, 2 forward GEMM, 3 dS/dB, 4 finalize dS/dB, 5 backward GEMM,
  * 6 dA, 7 finalize dA, 8 memset (gradients of adapters that own no rows),
- * 9-12 DoRA (U, norm, dZ, dmag).  Kind 6 runs on the library's side stream
- * beside the backward GEMM; its event pair spans from the fork to its end.
+ * 9-12 DoRA (U, norm, dZ, dmag).  When kind 6 runs on the library's side
+ * stream beside the backward GEMM, its event pair spans from the fork to its
+ * end.
  * Host-side cost: two event records per launch. */
 enum { LORA_KERNEL_KINDS = 13 };
 lora_status lora_timing_begin(void);

@@ -245,6 +245,10 @@ __global__ void __launch_bounds__(threads_of(G), 1) da_kernel(const __grid_const
                 }
                 bool ok = mbar_wait(&full[s], ph, w, 4);
                 if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                // bits handed over by the dX GEMM live in the workspace: zero them once they are in shared memory
+                if (p.bits_clear != nullptr && t < p.m)
+                    stg128(p.bits_clear + static_cast<int64_t>(t) * (p.k >> 3) + static_cast<int64_t>(d.fb) * 16,
+                           make_uint4(0u, 0u, 0u, 0u));
                 if (ad.T != 0u && p.use_bits) {
                     // the forward's keep bits: byte cc of the row's 16 covers chunk cc (bit e = feature 8 cc + e)
                     const uint32_t sbase = smem_u32(smem + s * p.stage_bytes);

@@ -311,6 +311,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         keep[c] |= keep_byte(philox_10(static_cast<uint32_t>(row), grp, keys), T) << (8 * g);
                     }
                 }
+                // hand the regenerated decisions to the dA pass (whole 16-byte groups: N % 128 == 0)
+                if (p.keep_out != nullptr && row < p.M) {
+                    uint8_t* kw = p.keep_out + row * (p.N >> 3) + (n0 >> 3);
+#pragma unroll
+                    for (int c = 0; c < BN / 32; c += 4)
+                        if (n0 + c * 32 < p.N) stg128(kw + c * 4, make_uint4(keep[c], keep[c + 1], keep[c + 2], keep[c + 3]));
+                }
             }
             const uint32_t b = C::kDouble ? (use & 1u) : 0u;
             const uint32_t full_parity = C::kDouble ? ((use >> 1) & 1u) : (use & 1u);

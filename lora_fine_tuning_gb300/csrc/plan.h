@@ -109,6 +109,8 @@ struct GemmParams {
     const float* col_scale;            // forward only, optional: output column j is multiplied by col_scale[j] (DoRA)
     const uint8_t* keep_bits;          // backward only, optional: the forward's keep bits (m x N/8 bytes, N % 32 == 0),
                                        // read instead of regenerating the mask
+    uint8_t* keep_out;                 // backward only, optional: where the regenerated keep bits of every branch row go
+                                       // (same layout; N % 128 == 0), for the dA pass to read
 };
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,
@@ -165,6 +167,7 @@ struct DaParams {
     CUtensorMap mapBits;               // optional: the forward's keep bits {k/8, m} bytes, box {16, 128}, no swizzle
     int32_t use_bits;                  // 1: the stage's keep bits come with X (at off_bits) instead of from Philox
     uint32_t off_bits;
+    uint8_t* bits_clear;               // optional: the bits tensor of mapBits, whose bytes this pass zeroes once read
     int32_t groups;                    // mask groups of four warps (2 or 3); stages % groups == 0
     Slots sl;                          // deterministic mode: dA partials per (adapter * nfb + feature block, CTA) slot
 };

@@ -78,3 +78,16 @@ def test_default_workload_is_the_70b_up_proj_rank_64(bench):
     fwd = M * K + K * N + M * N + K * R + R * N + M * R
     bwd = M * N + K * N + 2 * M * K + M * R + 2 * (K * R + R * N)
     assert wl.layer_bytes() == 2 * (fwd + bwd)
+
+
+def test_rank_pass_bytes_8b_up(bench):
+    """Algorithmic bytes behind the rank-r passes' HBM fractions: down_proj reads X, A and writes S'; ds_db
+    reads dY, S', B (dY twice in the deterministic mode); da reads X, the keep bits (one bit an element), dSq
+    and writes dA."""
+    wl = bench.Workload("llama8b_up")
+    assert wl.rank_bytes_per_step("down_proj") == 2 * m * k + 2 * k * r + 2 * m * r == 67_502_080
+    assert wl.rank_bytes_per_step("down_proj", saved_mask=True) == 67_502_080 + m * k // 8
+    assert wl.rank_bytes_per_step("ds_db") == 2 * m * n + 2 * m * r + 2 * r * n == 235_601_920
+    assert wl.rank_bytes_per_step("ds_db", deterministic=True) == 235_601_920 + 2 * m * n
+    assert wl.rank_bytes_per_step("da") == 2 * m * k + m * k // 8 + 2 * m * r + 2 * k * r == 71_696_384
+    assert wl.rank_bytes_per_step("gemm_fwd") is None
