@@ -267,8 +267,10 @@ struct Layout {
     size_t dsq = 0;         // m x s_ld bf16
     size_t acc = 0;         // per-adapter dB^T (n x rpad) and dA (k x rpad) fp32
     size_t acc_floats = 0;
-    size_t bits = 0;        // m x k/8 keep bits from the dX GEMM to the dA pass (k % 128 == 0; zeroed by dA)
     size_t slots = 0;       // deterministic mode only: partial sums of split items (cleared by their finalize)
+    size_t fwd_total = 0;   // bytes a forward call needs (the regions above)
+    size_t bits = 0;        // backward only: m x k/8 keep bits from the dX GEMM to the dA pass (k % 128 == 0;
+                            // zeroed by dA)
     size_t total = 0;
 };
 
@@ -300,14 +302,15 @@ Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int n
     for (int a = 0; a < nad; ++a) floats += static_cast<size_t>(n + k) * rpads[a];
     L.acc_floats = floats;
     off = up(off + floats * 4);
-    L.bits = off;
-    if (k % 128 == 0) off = up(off + static_cast<size_t>(m) * static_cast<size_t>(k / 8));
     if (det_ctas > 0) {
         int rpad_max = 16;
         for (int a = 0; a < nad; ++a) rpad_max = std::max(rpad_max, rpads[a]);
         L.slots = off;
         off = up(off + det_slot_bytes(m, k, std::max(s_ld, 8), rpad_max, nad, det_ctas));
     }
+    L.fwd_total = off;   // the forward uses nothing after this
+    L.bits = off;
+    if (k % 128 == 0) off = up(off + static_cast<size_t>(m) * static_cast<size_t>(k / 8));
     L.total = off;
     return L;
 }
@@ -386,7 +389,7 @@ lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_se
     }
     if (!workspace) return LORA_EWORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LORA_EWORKSPACE;
-    if (ws_bytes < c.L.total) return LORA_EWORKSPACE;
+    if (ws_bytes < (need_grads ? c.L.total : c.L.fwd_total)) return LORA_EWORKSPACE;
     c.ws = static_cast<uint8_t*>(workspace);
     st = device_setup(&c.sms);
     if (st) return st;
@@ -767,10 +770,9 @@ std::mutex g_static_mu;
 
 using namespace lora;
 
-extern "C" {
-
-size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters) {
-    if (m < 0 || k < 0 || n < 0 || r_max < 0 || n_adapters < 0) return 0;
+// The layout lora_workspace_size sizes: every adapter at rank r_max (upper bounds for any call with these sizes).
+Layout workspace_layout(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters) {
+    if (m < 0 || k < 0 || n < 0 || r_max < 0 || n_adapters < 0) return Layout{};
     int rp[kMaxAdapters];
     const int nad = std::min<int32_t>(std::max<int32_t>(n_adapters, 1), kMaxAdapters);
     for (int a = 0; a < nad; ++a) rp[a] = rank_pad(std::max(r_max, 8));
@@ -784,7 +786,13 @@ size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32
                        : 1024;
         cudaGetLastError();   // a failed query leaves no sticky error behind
     }
-    return layout(m, k, n, std::max(r_max, 8), rp, nad, det_ctas).total;
+    return layout(m, k, n, std::max(r_max, 8), rp, nad, det_ctas);
+}
+
+extern "C" {
+
+size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters) {
+    return workspace_layout(m, k, n, r_max, n_adapters).total;
 }
 
 lora_status lora_set_deterministic(int32_t on) {
@@ -859,7 +867,7 @@ lora_status lora_fwd_static_scratch(const lora_bf16* X, const lora_bf16* W, cons
     st = check_adapter(ad, false);
     if (st) return st;
     if ((m + kTileM - 1) / kTileM > kMaxTiles) return LORA_ESHAPE;
-    const size_t need = lora_workspace_size(m, k, n, r, 1);
+    const size_t need = workspace_layout(m, k, n, r, 1).fwd_total;   // a forward needs no backward-only region
     if (need > kStaticScratchBytes) {
         g_last_error = "lora_fwd_static_scratch: these sizes need more scratch than the 8 MiB static buffer";
         return LORA_EWORKSPACE;
