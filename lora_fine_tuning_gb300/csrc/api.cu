@@ -477,6 +477,9 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
     g.nkb = static_cast<int32_t>((k + 63) / 64);
     g.seed_lo = seed_lo;
     g.seed_hi = seed_hi;
+    // the down-projection, launched first, has waited on the caller's earlier work; no kernel of this call
+    // writes X or W, so the GEMM may start loading them before it waits on finalize_s
+    g.early_loads = (nad > 0 && c.rt.n_active > 0) ? 1 : 0;
     if (dora) {
         const lora_status st = run_dora_norm(c, *dora, W, ads[0], k, n);
         if (st) return st;
@@ -498,9 +501,11 @@ int bwd_tile_width(int64_t m, int64_t k, int64_t n) {
     return kBwdPairBN;
 }
 
+// dy_from_call: dY was written by an earlier kernel of the same call (DoRA's dZ), so the dX GEMM must not
+// read it before waiting on its predecessor.
 lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const uint16_t* W, const lora_adapter* ads,
                     uint64_t seed, int64_t m, int64_t k, int64_t n, const uint16_t* S_saved, const uint8_t* mask_bits,
-                    uint16_t* dX) {
+                    uint16_t* dX, bool dy_from_call = false) {
     const uint32_t seed_lo = static_cast<uint32_t>(seed), seed_hi = static_cast<uint32_t>(seed >> 32);
     const int nad = c.rt.n_adapters;
     uint16_t* dsq = reinterpret_cast<uint16_t*>(c.ws + c.L.dsq);
@@ -624,7 +629,10 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         // the forward's keep bits, when given, replace the epilogue's Philox (whole 32-bit words per row)
         g.keep_bits = (mask_bits != nullptr && k % 32 == 0) ? mask_bits : nullptr;
         g.keep_out = ws_bits;
-        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
+        // the dS/dB pass, launched first, has waited on the caller's earlier work; dY and W are written by no
+        // kernel of this call (unless dY is DoRA's dZ)
+        g.early_loads = (nad > 0 && c.rt.n_active > 0 && !dy_from_call) ? 1 : 0;
+            LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
     }
 
     if (fork_da || gemm_bits) {
@@ -1058,7 +1066,7 @@ lora_status dora_bwd(const lora_bf16* dY, const lora_bf16* X, const lora_bf16* W
     if (m > 0)
         LORA_CUDA(timed(kDoraDz, c.stream, [&] { return launch_dora_dz(dY, Y, g_saved, m, n, dZ, dmag_acc, c.sms,
                                                                       c.stream); }));
-    st = run_bwd(c, dZ, X, W, &ad, seed, m, k, n, S_saved, mask_bits, dX);
+    st = run_bwd(c, dZ, X, W, &ad, seed, m, k, n, S_saved, mask_bits, dX, /*dy_from_call=*/true);
     if (st) return st;
     LORA_CUDA(timed(kDoraDmag, c.stream, [&] { return launch_dora_dmag(dmag_acc, mag, n, dmag, c.stream); }));
     return LORA_OK;

@@ -132,7 +132,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_fence_before();
     cluster_sync();   // barriers initialised and TMEM allocated in both CTAs
     tc_fence_after();
-    pdl_wait();
+    // Programmatic dependent launch: wait for the previous kernel before touching what it may write.  With
+    // early_loads the producer first streams the first tile's main-loop stages (operands no earlier kernel of
+    // the call writes) and waits afterwards; the MMA thread touches no global memory, and the epilogue waits
+    // before its first global access.
+    const bool early = p.early_loads != 0;
+    if (!early) pdl_wait();
     pdl_trigger();
     const uint32_t tmem = *tmem_slot;
     const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, (kBwd ? kKGemmBwd : kKGemmFwd) << 8};
@@ -150,6 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             int64_t issued = 0;
             bool ok = true;
+            bool waited = !early;
             for (int tile = pair; tile < total && ok; tile += npairs) {
                 const PairTile pt = pair_tile<BN>(tile, p);
                 const int m0 = pt.mp * 256 + static_cast<int>(rank) * 128;
@@ -157,6 +163,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const Tail tl = tail_of(pt.mp, p);
                 const int my_adapter = tl.half_adapter[rank];
                 for (int kb = 0; kb < nkb + tl.total; ++kb) {
+                    // only the first ring's worth of main-loop stages of the first tile go before the wait
+                    if (!waited && (tile != pair || kb >= nkb || issued >= S)) {
+                        pdl_wait();
+                        waited = true;
+                    }
                     if (!mbar_wait_cl(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
                     uint8_t* as = smem + s * C::kStage;
                     uint8_t* bs = as + C::kA;
@@ -199,6 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
             }
+            if (!waited) pdl_wait();
             if (!ok && leader) {
                 const int64_t back = issued < S ? issued : S;
                 for (int64_t i = issued - back; i < issued; ++i)
@@ -278,6 +290,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int quad = warp & 3;
         const int er = quad * 32 + lane;   // row within this CTA's 128 rows (= TMEM lane)
         const bool issuer = warp == 2 && lane == 0;
+        if (early) pdl_wait();   // before the keep bits, the column scale and the stores
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
         uint32_t use = 0;
         int sb = 0;

@@ -111,6 +111,9 @@ struct GemmParams {
                                        // read instead of regenerating the mask
     uint8_t* keep_out;                 // backward only, optional: where the regenerated keep bits of every branch row go
                                        // (same layout; N % 128 == 0), for the dA pass to read
+    int32_t early_loads;               // 1: the producer may load the first tile's main-loop stages before waiting on
+                                       // the previous kernel (no kernel of this call writes the main-loop operands, and
+                                       // an earlier kernel of the call has already waited on the caller's work)
 };
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,

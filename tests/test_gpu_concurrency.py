@@ -1,8 +1,8 @@
 """Calls from several host threads on several streams at once.
 
 Each entry point prepares its launches in per-thread storage and takes no lock
-while it enqueues, and each caller stream has its own side stream for the dA
-pass.  Two threads run forward + backward steps of different layers on their
+while it enqueues, and each caller stream has its own side stream for a forked
+dA pass.  Two threads run forward + backward steps of different layers on their
 own streams and workspaces at the same time; every result must match the same
 step run alone (keep masks bit-exact, values within the parity tolerance).
 """
@@ -21,7 +21,9 @@ if not torch.cuda.is_available():  # pragma: no cover
 
 from lora_fine_tuning_gb300 import api  # noqa: E402
 
-CASES = [(512, 1024, 768, 16, 2.0, 0.1, 91), (384, 768, 1024, 64, 1.0, 0.2, 92)]
+# k % 128 != 0 in both layers: each backward forks its dA pass onto its own stream's side stream (with
+# k % 128 == 0 the dA pass reads the dX GEMM's keep bits on the caller's stream and nothing is shared)
+CASES = [(512, 1032, 768, 16, 2.0, 0.1, 91), (384, 776, 1024, 64, 1.0, 0.2, 92)]
 
 
 def make(case):

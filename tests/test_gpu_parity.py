@@ -58,7 +58,8 @@ def test_tiny_workload():
     (256, 4096, 320, 16, 2.0, 0.1, 2**33 + 5),  # many k blocks: a tile split over CTAs; seed above 2^32
     (640, 192, 2048, 32, 4.0, 0.5, 15),      # many n blocks in the dS/dB pass
     (1, 64, 64, 16, 1.0, 0.1, 16),           # one row
-    (2048, 8192, 64, 16, 2.0, 0.1, 17),      # short dX GEMM (K = 64), long dA pass beside it: the join must wait
+    (2048, 8192, 64, 16, 2.0, 0.1, 17),      # short dX GEMM (K = 64); the dA pass then reads the bits it wrote
+    (2048, 8184, 64, 16, 2.0, 0.1, 18),      # k % 128 != 0: a long dA pass forked beside the short GEMM, the join must wait
 ])
 def test_single_shapes(m, k, n, r, alpha, p, seed):
     raw, out = run_single(m, k, n, r, alpha, p, seed)
@@ -287,10 +288,12 @@ def test_stuck_wait_reports_timeout_and_context_survives():
     check_single_full(raw, out, 1.0, 0.1, 5)
 
 
-@pytest.mark.parametrize("m,k,n,r,saved_bits", [(640, 1032, 392, 24, False), (640, 1024, 392, 24, True)])
+@pytest.mark.parametrize("m,k,n,r,saved_bits", [(640, 1032, 392, 24, False), (640, 1024, 392, 24, True),
+                                                  (640, 1024, 392, 24, False)])
 def test_workspace_is_left_zeroed(m, k, n, r, saved_bits):
-    """Each call leaves the workspace all zeros, so calls of any shape can share it (also when the backward
-    reads the forward's keep bits: k % 128 == 0 takes the bits path in both backward kernels)."""
+    """Each call leaves the workspace all zeros, so calls of any shape can share it: with k % 128 != 0 (the dA
+    pass regenerates the mask beside the dX GEMM), with the forward's keep bits, and with the keep bits the
+    dX GEMM hands to the dA pass in the workspace (k % 128 == 0, none given)."""
     raw = synth.layer_inputs(51, m, k, n, r)
     X, W, A, B, dY = (to_dev(raw[x]) for x in ("X", "W", "A", "B", "dY"))
     ws = torch.zeros(api.lora_workspace_size(m, k, n, r), dtype=torch.uint8, device="cuda")
