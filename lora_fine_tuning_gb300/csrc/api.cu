@@ -632,7 +632,7 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         // the dS/dB pass, launched first, has waited on the caller's earlier work; dY and W are written by no
         // kernel of this call (unless dY is DoRA's dZ)
         g.early_loads = (nad > 0 && c.rt.n_active > 0 && !dy_from_call) ? 1 : 0;
-            LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
+        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
     }
 
     if (fork_da || gemm_bits) {
