@@ -876,12 +876,12 @@ def run_native(args):
         for label, fn in (("ours", prob.frozen_step), ("torch_matmul", prob.torch_frozen_step)):
             fn()
             torch.cuda.synchronize(dev)
-            if label == "ours":
-                native.timing_begin()
-            ms = timed_loop(fn, reps, stream, flush)
-            if label == "ours":
-                frozen_kernels = {kname: t / max(1, cnt) for kname, (t, cnt) in native.timing_end().items()}
-            res[label] = max_over_ranks(ms) / reps
+            res[label] = max_over_ranks(timed_loop(fn, reps, stream, flush)) / reps
+        # per-launch times from a separate loop: the events between launches would otherwise be in the
+        # frozen step's own time (they also keep consecutive kernels from overlapping)
+        native.timing_begin()
+        timed_loop(prob.frozen_step, min(reps, 20), stream, flush)
+        frozen_kernels = {kname: t / max(1, cnt) for kname, (t, cnt) in native.timing_end().items()}
         frozen = {"frozen_ms_per_step_ours": res["ours"], "frozen_ms_per_step_torch": res["torch_matmul"],
                   "frozen_ms_per_launch_ours": frozen_kernels,
                   "lora_overhead_vs_ours": ms_per_step / res["ours"],

@@ -113,7 +113,16 @@ typedef struct {
 /* Workspace bytes sufficient for every call below with these sizes
  * (r_max: the largest rank; n_adapters: adapters per call, >= 1), in the
  * current reduction mode (lora_set_deterministic): the deterministic mode
- * needs a larger workspace, sized for the current device. */
+ * needs a larger workspace, sized for the current device.
+ *
+ * The last region of this size holds the partial sums of GEMM output tiles
+ * whose K loop is split over several CTA pairs (up to 80 pairs x 256 KB, 20
+ * MB; less when the GEMMs have few tiles).  A call whose workspace ends before
+ * that region still runs, with every tile computed whole by one pair: the GEMMs
+ * then leave more CTA pairs idle when their last wave of tiles is nearly empty.
+ * Results with and without the region agree to fp32 rounding; the split sums
+ * are added in a fixed order, so either form is bit-reproducible in the
+ * deterministic mode. */
 size_t lora_workspace_size(int64_t m, int64_t k, int64_t n, int32_t r_max, int32_t n_adapters);
 
 /* Reduction mode of every later call in this process (0 by default).
@@ -299,6 +308,22 @@ void lora_set_wait_limit_ns(uint64_t ns);
  * barrier nothing will complete, with the current limit, and returns.  The
  * device status then reads LORA_EDEVICE_TIMEOUT; the context stays usable. */
 lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void* stream);
+
+/* Test hook for the schedule of the CTA-pair GEMMs (host only; no device is
+ * needed).  For an M x N output in tiles of 256 rows x bn columns, `stages`
+ * 64-deep K stages a tile, at most `max_pairs` CTA pairs (half the SMs),
+ * tile splitting allowed (allow_split != 0) or not, and one accumulator set
+ * per CTA (single_acc != 0: the 256-wide backward GEMM) or two, *pairs
+ * receives the grid's pair count and *split_tiles the number of tiles split
+ * by K.  Run i of the schedule is written to runs[4i .. 4i+3] as (pair, tile,
+ * first stage, end stage) for i < cap, pairs in order and each pair's runs in
+ * the order it works through them; *n_runs receives the number of runs.  A
+ * split tile's stages are spread over several runs: the run holding stage 0
+ * adds the others' partial sums and stores the tile.  LORA_EINVAL for
+ * missing pointers or arguments below 1 (cap below 0). */
+lora_status lora_debug_gemm_runs(int64_t M, int64_t N, int32_t bn, int32_t stages, int32_t max_pairs,
+                                 int32_t allow_split, int32_t single_acc, int32_t* pairs, int32_t* split_tiles,
+                                 int32_t* runs, int64_t cap, int64_t* n_runs);
 
 const char* lora_status_string(lora_status s);
 

@@ -271,8 +271,23 @@ struct Layout {
     size_t fwd_total = 0;   // bytes a forward call needs (the regions above)
     size_t bits = 0;        // backward only: m x k/8 keep bits from the dX GEMM to the dA pass (k % 128 == 0;
                             // zeroed by dA)
+    size_t grads_total = 0; // bytes a backward call needs (the regions above)
+    size_t sk = 0;          // optional: the pair GEMMs' split-tile flags, then their partial slots (plan.h); the
+                            // closing run of a split tile resets the flags and zeroes the slots it reads
+    int32_t sk_pairs = 0;   // pairs with a slot
     size_t total = 0;
 };
+
+// Pairs that may hold a split-tile partial: a GEMM splits tiles over at most twice its tile count of pairs,
+// and never over more pairs than kSkSlotPairs (on a device with more SMs the GEMMs split no tiles).
+constexpr int kSkSlotPairs = 80;
+
+int32_t sk_slot_pairs(int64_t m, int64_t k, int64_t n) {
+    const int64_t tiles = ((m + 255) / 256) * ((std::max(k, n) + 127) / 128);   // 128 wide: an upper bound
+    return static_cast<int32_t>(std::min<int64_t>(kSkSlotPairs, 2 * tiles));
+}
+
+size_t sk_flag_bytes(int32_t pairs) { return up(static_cast<size_t>(pairs) * 2 * 4); }
 
 // Deterministic mode: bytes of the slot region, whose slots (128 rows each) hold the partial sums of output
 // items split over CTAs (plan.h, Slots): S' and dS items are active tiles (s_ld floats a row), dA items are
@@ -308,9 +323,13 @@ Layout layout(int64_t m, int64_t k, int64_t n, int s_ld, const int* rpads, int n
         L.slots = off;
         off = up(off + det_slot_bytes(m, k, std::max(s_ld, 8), rpad_max, nad, det_ctas));
     }
-    L.fwd_total = off;   // the forward uses nothing after this
+    L.fwd_total = off;   // the forward needs nothing after this
     L.bits = off;
     if (k % 128 == 0) off = up(off + static_cast<size_t>(m) * static_cast<size_t>(k / 8));
+    L.grads_total = off;
+    L.sk = off;
+    L.sk_pairs = sk_slot_pairs(m, k, n);
+    off = up(off + sk_flag_bytes(L.sk_pairs) + static_cast<size_t>(L.sk_pairs) * 2 * kSkSlotFloats * 4);
     L.total = off;
     return L;
 }
@@ -327,6 +346,7 @@ struct Call {
     uint8_t* ws = nullptr;
     int sms = 0;
     bool det = false;    // deterministic mode for this call
+    bool sk = false;     // the workspace holds the split-tile region
     cudaStream_t stream = nullptr;
 };
 
@@ -389,7 +409,8 @@ lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_se
     }
     if (!workspace) return LORA_EWORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) % kAlign) return LORA_EWORKSPACE;
-    if (ws_bytes < (need_grads ? c.L.total : c.L.fwd_total)) return LORA_EWORKSPACE;
+    if (ws_bytes < (need_grads ? c.L.grads_total : c.L.fwd_total)) return LORA_EWORKSPACE;
+    c.sk = ws_bytes >= c.L.total;
     c.ws = static_cast<uint8_t*>(workspace);
     st = device_setup(&c.sms);
     if (st) return st;
@@ -398,6 +419,16 @@ lora_status prepare(Call& c, const lora_adapter* ads, int32_t nad, const lora_se
 }
 
 DevCtl ctl_of(const Call& c) { return DevCtl{reinterpret_cast<int*>(c.ws + c.L.status), g_wait_ns}; }
+
+// Grid of a pair GEMM and its split tiles: splits only where the workspace holds slots for every pair.
+GemmSched gemm_plan(const Call& c, GemmParams& g, bool bwd, int bn) {
+    GemmSched sc = plan_gemm2(g, bwd, bn, c.sms, c.sk);
+    if (sc.sk_tiles > 0 && sc.pairs > c.L.sk_pairs) sc = plan_gemm2(g, bwd, bn, c.sms, false);
+    g.sk_tiles = sc.sk_tiles;
+    g.sk_flag = reinterpret_cast<uint32_t*>(c.ws + c.L.sk);
+    g.sk_part = reinterpret_cast<float*>(c.ws + c.L.sk + sk_flag_bytes(c.L.sk_pairs));
+    return sc;
+}
 
 #define LORA_CUDA(expr)                          \
     do {                                         \
@@ -485,7 +516,8 @@ lora_status run_fwd(const Call& c, const uint16_t* X, const uint16_t* W, const l
         if (st) return st;
         g.col_scale = dora->g_out;
     }
-    LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm2(g, false, 256, c.sms, c.stream); }));
+    const GemmSched sc = gemm_plan(c, g, false, 256);
+    LORA_CUDA(timed(kGemmFwd, c.stream, [&] { return launch_gemm2(g, false, 256, sc.pairs, c.stream); }));
     return LORA_OK;
 }
 
@@ -632,7 +664,8 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         // the dS/dB pass, launched first, has waited on the caller's earlier work; dY and W are written by no
         // kernel of this call (unless dY is DoRA's dZ)
         g.early_loads = (nad > 0 && c.rt.n_active > 0 && !dy_from_call) ? 1 : 0;
-        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, c.sms, c.stream); }));
+        const GemmSched sc = gemm_plan(c, g, true, bn);
+        LORA_CUDA(timed(kGemmBwd, c.stream, [&] { return launch_gemm2(g, true, bn, sc.pairs, c.stream); }));
     }
 
     if (fork_da || gemm_bits) {
@@ -947,6 +980,31 @@ lora_status lora_debug_stuck_wait(void* workspace, size_t workspace_bytes, void*
     if (st) return st;
     DevCtl ctl{static_cast<int*>(workspace), g_wait_ns};
     if (!cuda_ok(launch_stuck_wait(ctl, static_cast<cudaStream_t>(stream)))) return LORA_ECUDA;
+    return LORA_OK;
+}
+
+lora_status lora_debug_gemm_runs(int64_t M, int64_t N, int32_t bn, int32_t stages, int32_t max_pairs,
+                                 int32_t allow_split, int32_t single_acc, int32_t* pairs, int32_t* split_tiles,
+                                 int32_t* runs, int64_t cap, int64_t* n_runs) {
+    if (!pairs || !split_tiles || !n_runs || (cap > 0 && !runs)) return LORA_EINVAL;
+    if (M < 1 || N < 1 || bn < 1 || stages < 1 || max_pairs < 1 || cap < 0) return LORA_EINVAL;
+    const int64_t T = ((M + 255) / 256) * ((N + bn - 1) / bn);
+    if (T > (int64_t{1} << 30)) return LORA_EINVAL;
+    const GemmSched sc = gemm_schedule(M, N, bn, stages, max_pairs, allow_split != 0, single_acc != 0);
+    *pairs = sc.pairs;
+    *split_tiles = sc.sk_tiles;
+    int64_t n = 0;
+    for (int c = 0; c < sc.pairs; ++c) {
+        RunWalk w = run_walk(sc.sk_tiles, c, sc.pairs, stages, static_cast<int>(T));
+        for (Run r; w.next(r); ++n) {
+            if (n >= cap) continue;
+            runs[4 * n] = c;
+            runs[4 * n + 1] = r.tile;
+            runs[4 * n + 2] = r.kb0;
+            runs[4 * n + 3] = r.kb1;
+        }
+    }
+    *n_runs = n;
     return LORA_OK;
 }
 

@@ -127,6 +127,36 @@ static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t pari
     return true;
 }
 
+// Flags between CTAs of one grid, in global memory (gpu scope).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Bounded wait until *flag is non-zero (acquire).  The flag is set by another CTA of the same grid that
+// needs nothing from this one; false if the CTA is aborting or the wait ran out of time.
+static __device__ __noinline__ bool flag_wait(const uint32_t* flag, const WaitCtx& w, int site) {
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i) {
+            if (ld_acquire_gpu(flag) != 0) return true;
+            __nanosleep(100);
+        }
+        if (*w.abort) return false;
+        if (global_timer_ns() - t0 > w.limit_ns) {
+            *w.abort = 1;
+            if (w.status) atomicCAS(w.status, 0, w.code | site);
+            return false;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // TMA (bulk tensor copies global -> shared, completion on an mbarrier)
 // ---------------------------------------------------------------------------

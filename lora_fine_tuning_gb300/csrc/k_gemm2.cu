@@ -23,6 +23,13 @@
 // only) and TMEM allocation, warps 2-5 epilogue (both CTAs, own rows): the
 // output goes through a swizzled shared-memory block and a TMA tensor store,
 // so global writes are whole 128-byte lines.
+//
+// Every role walks the same runs (plan.h): whole tiles, and where a last wave
+// of tiles would leave most pairs idle, first a stream-K part in which tiles
+// are cut into runs of K stages spread evenly over the pairs.  The rank-r
+// tail goes with the run that ends a tile's K loop.  A run that does not start
+// its tile hands its fp32 sum to the run that does through a partial slot and
+// a flag in the workspace.
 #include "cluster.cuh"
 #include "kernels.h"
 
@@ -84,6 +91,59 @@ __device__ __forceinline__ PairTile pair_tile(int tile, const GemmParams& p) {
     const int gm = min(n_mp - first, kGroupPairs);
     const int in_group = tile - group * per_group;
     return PairTile{first + in_group % gm, in_group / gm};
+}
+
+__device__ __forceinline__ RunWalk pair_runs(const GemmParams& p, int pair, int npairs, int nk, int total) {
+    return run_walk(p.sk_tiles, pair, npairs, nk, total);
+}
+
+// 16 accumulator columns of this thread's row; with the branch, plus the second accumulator's where the
+// keep bits say the element was kept.
+template <int BN>
+__device__ __forceinline__ void acc_chunk(uint32_t t1, uint32_t t2, int c, bool branch, const uint32_t (&keep)[BN / 32],
+                                          uint32_t (&v)[16]) {
+    tmem_ld16(t1 + c * 16, v);
+    if (branch) {
+        uint32_t u[16];
+        tmem_ld16(t2 + c * 16, u);
+        tmem_ld_wait();
+        const uint32_t kb = keep[c >> 1] >> ((c & 1) * 16);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            if ((kb >> e) & 1u) v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
+    } else {
+        tmem_ld_wait();
+    }
+}
+
+// DoRA: column j of the output times g_j (columns past N read nothing; the store clips them).
+__device__ __forceinline__ void col_scale_chunk(const GemmParams& p, int col0, float* f) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+        const int64_t col = static_cast<int64_t>(col0) + e;
+        f[e] *= col < p.N ? __ldg(p.col_scale + col) : 0.f;
+    }
+}
+
+// One 128 x 64 bf16 block of the output (this thread's row: 32 packed words) through a 128B-swizzled
+// staging buffer and a TMA store; the two buffers alternate.
+__device__ __forceinline__ void store_block(const CUtensorMap& map, uint8_t* staging, int& sb, bool issuer, int er,
+                                            const uint32_t* pk, int x, int y) {
+    uint8_t* buf = staging + sb * 16384;
+    // the store that last read this buffer (two blocks ago) must be done with it
+    if (issuer) bulk_wait_read<1>();
+    named_barrier(1, 128);
+    const uint32_t rowbase = smem_u32(buf) + er * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)   // 16-byte chunk j of the row's 128 bytes
+        sts128(rowbase + ((j ^ (er & 7)) << 4), make_uint4(pk[j * 4], pk[j * 4 + 1], pk[j * 4 + 2], pk[j * 4 + 3]));
+    fence_proxy_async_smem();
+    named_barrier(1, 128);
+    if (issuer) {
+        tma_store_2d(&map, buf, x, y);
+        bulk_commit();
+    }
+    sb ^= 1;
 }
 
 template <bool kBwd, int BN>
@@ -156,15 +216,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             bool waited = !early;
-            for (int tile = pair; tile < total && ok; tile += npairs) {
-                const PairTile pt = pair_tile<BN>(tile, p);
+            bool first_run = true;
+            RunWalk rw = pair_runs(p, pair, npairs, nkb, total);
+            for (Run run; ok && rw.next(run); first_run = false) {
+                const PairTile pt = pair_tile<BN>(run.tile, p);
                 const int m0 = pt.mp * 256 + static_cast<int>(rank) * 128;
                 const int n0 = pt.np * BN + static_cast<int>(rank) * C::BNH;
                 const Tail tl = tail_of(pt.mp, p);
                 const int my_adapter = tl.half_adapter[rank];
-                for (int kb = 0; kb < nkb + tl.total; ++kb) {
-                    // only the first ring's worth of main-loop stages of the first tile go before the wait
-                    if (!waited && (tile != pair || kb >= nkb || issued >= S)) {
+                const int ntail = run.kb1 == nkb ? tl.total : 0;
+                for (int j = run.kb0; j < run.kb1 + ntail; ++j) {
+                    // only the first ring's worth of main-loop stages of the first run go before the wait
+                    if (!waited && (!first_run || j >= run.kb1 || issued >= S)) {
                         pdl_wait();
                         waited = true;
                     }
@@ -174,10 +237,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(&full[s], 2u * C::kStage);
                     const uint32_t fb = peer_addr(smem_u32(&full[s]), 0);
                     // kKB boxes of 64 K per operand; a box past the end of K reads zeros
-                    if (kb < nkb) {
+                    if (j < run.kb1) {
 #pragma unroll
                         for (int q = 0; q < kKB; ++q) {
-                            const int x = kb * kBK + 64 * q;
+                            const int x = j * kBK + 64 * q;
                             tma_load_2d_pair(as + q * 16384, &p.mapA, fb, x, m0);
                             if (kBwd) {
                                 tma_load_2d_pair(bs + q * C::kBox, &p.mapB, fb, x, n0);
@@ -188,7 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                             }
                         }
                     } else {
-                        const int t = kb - nkb;
+                        const int t = j - run.kb1;
                         const int pass = t < tl.nb[0] ? 0 : 1;
                         const int tb = pass == 0 ? t : t - tl.nb[0];
                         const int a = tl.a[pass];
@@ -235,27 +298,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const auto a_step = [](int ks) -> uint64_t { return (ks >> 2) * (16384u >> 4) + (ks & 3) * 2u; };
             const auto b_step = [](int ks) -> uint64_t { return (ks >> 2) * (C::kBox >> 4) + (ks & 3) * kBStep; };
             bool ok = true;
-            for (int tile = pair; tile < total && ok; tile += npairs) {
-                const PairTile pt = pair_tile<BN>(tile, p);
+            RunWalk rw = pair_runs(p, pair, npairs, nkb, total);
+            for (Run run; ok && rw.next(run);) {
+                const PairTile pt = pair_tile<BN>(run.tile, p);
                 const Tail tl = tail_of(pt.mp, p);
+                const int ntail = run.kb1 == nkb ? tl.total : 0;
                 const uint32_t b = C::kDouble ? (use & 1u) : 0u;
                 const uint32_t empty_parity = C::kDouble ? (((use >> 1) & 1u) ^ 1u) : ((use & 1u) ^ 1u);
                 if (!mbar_wait_cl(&acc_empty[b], empty_parity, w, 2)) break;
                 tc_fence_after();
                 const uint32_t acc1 = tmem + b * C::kBufCols;
                 const uint32_t acc2 = acc1 + BN;
-                for (int kb = 0; kb < nkb; ++kb) {
+                for (int kb = run.kb0; kb < run.kb1; ++kb) {
                     if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
-                    umma_bf16_pair(acc1, a_desc0 + so, b_desc0 + so, idesc, kb != 0 ? 1u : 0u);
+                    umma_bf16_pair(acc1, a_desc0 + so, b_desc0 + so, idesc, kb != run.kb0 ? 1u : 0u);
 #pragma unroll
                     for (int ks = 1; ks < 4 * kKB; ++ks)
                         umma_bf16_pair(acc1, a_desc0 + so + a_step(ks), b_desc0 + so + b_step(ks), idesc, 1u);
                     umma_commit_pair(&empty[s], 3);
                     if (++s == S) { s = 0; ph ^= 1u; }
                 }
-                for (int t = 0; t < tl.total && ok; ++t) {
+                for (int t = 0; t < ntail && ok; ++t) {
                     if (!mbar_wait_cl(&full[s], ph, w, 3)) { ok = false; break; }
                     tc_fence_after();
                     const uint64_t so = static_cast<uint64_t>(s) * (C::kStage >> 4);
@@ -287,21 +352,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // anything is stored.  Then 128B-swizzled staging blocks of 128 rows x 64
         // columns, one TMA store each (two staging buffers, so storing one block
         // overlaps filling the next).
+        //
+        // Split tiles: a run that does not start its tile stores its fp32 sum (with the masked branch term
+        // when it holds the tail) to its pair's partial slot and raises the pair's flag.  The run that starts
+        // the tile waits for the flags of the pairs holding the rest, adds their partials to its own
+        // accumulator in pair order (the same order on every call), clears the slots and stores the tile.
         const int quad = warp & 3;
         const int er = quad * 32 + lane;   // row within this CTA's 128 rows (= TMEM lane)
         const bool issuer = warp == 2 && lane == 0;
         if (early) pdl_wait();   // before the keep bits, the column scale and the stores
         const PhiloxKeys keys = philox_keys(p.seed_lo, p.seed_hi);
+        const int64_t U = static_cast<int64_t>(p.sk_tiles) * nkb;
         uint32_t use = 0;
         int sb = 0;
         if (issuer) tma_prefetch_desc(&p.mapOut);
-        for (int tile = pair; tile < total; tile += npairs) {
-            const PairTile pt = pair_tile<BN>(tile, p);
+        RunWalk rw = pair_runs(p, pair, npairs, nkb, total);
+        for (Run run; rw.next(run);) {
+            const PairTile pt = pair_tile<BN>(run.tile, p);
             const Tail tl = tail_of(pt.mp, p);
             const int m0 = pt.mp * 256 + static_cast<int>(rank) * 128;
             const int n0 = pt.np * BN;
             const int a = tl.half_adapter[rank];
-            const bool branch = kBwd && a >= 0;
+            const bool has_tail = run.kb1 == nkb;
+            const bool split = run.kb0 > 0 || !has_tail;
+            const bool branch = kBwd && a >= 0 && has_tail;
             const int64_t row = static_cast<int64_t>(m0) + er;
             uint32_t keep[BN / 32];
 #pragma unroll
@@ -332,69 +406,120 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         if (n0 + c * 32 < p.N) stg128(kw + c * 4, make_uint4(keep[c], keep[c + 1], keep[c + 2], keep[c + 3]));
                 }
             }
+            // a split tile's first run: the pairs after this one whose first runs hold the rest of the tile
+            const bool closing = split && run.kb0 == 0;
+            int parts = 0;
+            bool flags_ok = true;
+            if (closing) {
+                const int64_t tile_end = static_cast<int64_t>(run.tile + 1) * nkb;
+                while (parts < kSkMaxParts && sk_unit_begin(pair + 1 + parts, U, npairs) < tile_end) ++parts;
+                if (issuer) {
+                    if (sk_unit_begin(pair + 1 + parts, U, npairs) < tile_end) {   // more runs than slots: refuse
+                        abort_flag = 1;
+                        if (p.ctl.status) atomicCAS(p.ctl.status, 0, w.code | 6);
+                        flags_ok = false;
+                    }
+                    for (int j = 0; j < parts && flags_ok; ++j)
+                        flags_ok = flag_wait(p.sk_flag + (pair + 1 + j) * 2 + rank, w, 5);
+                }
+            }
             const uint32_t b = C::kDouble ? (use & 1u) : 0u;
             const uint32_t full_parity = C::kDouble ? ((use >> 1) & 1u) : (use & 1u);
             const bool ok = mbar_wait_cl(&acc_full[b], full_parity, w, 4);
             // every epilogue thread has finished its (bounded) wait; all four warps
             // leave together if any of them timed out or the CTA is aborting
-            if (named_barrier_or(1, 128, !ok || abort_flag != 0)) break;
+            if (named_barrier_or(1, 128, !ok || !flags_ok || abort_flag != 0)) break;
             tc_fence_after();
             const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
             const uint32_t t1 = tmem + lane_off + b * C::kBufCols;
             const uint32_t t2 = t1 + BN;
-            uint32_t packed[BN / 2];
+            if (split && !closing) {
+                // the rest of a split tile: fp32 partial to this pair's slot, 16-byte pieces laid out so that a
+                // warp's stores of one piece index cover 512 contiguous bytes
+                float* slot = p.sk_part + (static_cast<size_t>(pair) * 2 + rank) * kSkSlotFloats;
 #pragma unroll
-            for (int c = 0; c < BN / 16; ++c) {
-                uint32_t v[16];
-                tmem_ld16(t1 + c * 16, v);
-                if (branch) {
-                    uint32_t u[16];
-                    tmem_ld16(t2 + c * 16, u);
-                    tmem_ld_wait();
-                    const uint32_t kb = keep[c >> 1] >> ((c & 1) * 16);
+                for (int c = 0; c < BN / 16; ++c) {
+                    uint32_t v[16];
+                    acc_chunk<BN>(t1, t2, c, branch, keep, v);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if ((kb >> e) & 1u)
-                            v[e] = __float_as_uint(__uint_as_float(v[e]) + __uint_as_float(u[e]));
-                } else {
-                    tmem_ld_wait();
+                    for (int q = 0; q < 4; ++q)
+                        st_f4(slot + ((c * 4 + q) * 128 + er) * 4, __uint_as_float(v[4 * q]),
+                              __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                              __uint_as_float(v[4 * q + 3]));
                 }
-                if (!kBwd && p.col_scale != nullptr) {
-                    // DoRA: column j of the output times g_j (columns past N read nothing; the store clips them)
+                tc_fence_before();
+                mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+                __threadfence();            // this thread's partial is visible at gpu scope ...
+                named_barrier(1, 128);      // ... and so is every other thread's
+                if (issuer) st_release_gpu(p.sk_flag + pair * 2 + rank, 1u);
+            } else if (closing) {
+                // own accumulator + the other runs' partials, in pair order; 64 columns at a time
+#pragma unroll 1
+                for (int j = 0; j < parts; ++j) (void)ld_acquire_gpu(p.sk_flag + (pair + 1 + j) * 2 + rank);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int64_t col = static_cast<int64_t>(n0) + c * 16 + e;
-                        const float gsc = col < p.N ? __ldg(p.col_scale + col) : 0.f;
-                        v[e] = __float_as_uint(__uint_as_float(v[e]) * gsc);
+                for (int blk = 0; blk < BN / 64; ++blk) {
+                    const float* src0 = p.sk_part + (static_cast<size_t>(pair + 1) * 2 + rank) * kSkSlotFloats;
+                    float4 pf[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pf[i] = ld_l2_f4(src0 + ((blk * 16 + i) * 128 + er) * 4);
+                    float acc[64];
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        uint32_t v[16];
+                        tmem_ld16(t1 + (blk * 4 + c4) * 16, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) acc[c4 * 16 + e] = __uint_as_float(v[e]);
                     }
-                }
+                    if (blk == BN / 64 - 1) {
+                        // all of this tile's TMEM reads are done: hand the accumulator back
+                        tc_fence_before();
+                        mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+                    }
+                    for (int j = 0; j < parts; ++j) {
+                        const float* src = p.sk_part + (static_cast<size_t>(pair + 1 + j) * 2 + rank) * kSkSlotFloats;
+                        if (j > 0) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    packed[c * 8 + e] = pack_bf16x2(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-            }
-            // all of this tile's TMEM reads are done: hand the accumulator back
-            tc_fence_before();
-            mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+                            for (int i = 0; i < 16; ++i) pf[i] = ld_l2_f4(src + ((blk * 16 + i) * 128 + er) * 4);
+                        }
 #pragma unroll
-            for (int blk = 0; blk < BN / 64; ++blk) {
-                uint8_t* buf = staging + sb * 16384;
-                // the store that last read this buffer (two blocks ago) must be done with it
-                if (issuer) bulk_wait_read<1>();
-                named_barrier(1, 128);
-                const uint32_t rowbase = smem_u32(buf) + er * 128;
+                        for (int i = 0; i < 16; ++i) {
+                            acc[4 * i] += pf[i].x;
+                            acc[4 * i + 1] += pf[i].y;
+                            acc[4 * i + 2] += pf[i].z;
+                            acc[4 * i + 3] += pf[i].w;
+                            st_zero_f4(const_cast<float*>(src) + ((blk * 16 + i) * 128 + er) * 4);
+                        }
+                    }
+                    uint32_t pk[32];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {   // 16-byte chunk j of the row's 128 bytes
-                    const uint4 pk = make_uint4(packed[blk * 32 + j * 4 + 0], packed[blk * 32 + j * 4 + 1],
-                                                packed[blk * 32 + j * 4 + 2], packed[blk * 32 + j * 4 + 3]);
-                    sts128(rowbase + ((j ^ (er & 7)) << 4), pk);
+                    for (int c4 = 0; c4 < 4; ++c4) {
+                        if (!kBwd && p.col_scale != nullptr) col_scale_chunk(p, n0 + blk * 64 + c4 * 16, acc + c4 * 16);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) pk[c4 * 8 + e] = pack_bf16x2(acc[c4 * 16 + 2 * e], acc[c4 * 16 + 2 * e + 1]);
+                    }
+                    store_block(p.mapOut, staging, sb, issuer, er, pk, n0 + blk * 64, m0);
                 }
-                fence_proxy_async_smem();
-                named_barrier(1, 128);
-                if (issuer) {
-                    tma_store_2d(&p.mapOut, buf, n0 + blk * 64, m0);
-                    bulk_commit();
+                if (issuer)
+                    for (int j = 0; j < parts; ++j) p.sk_flag[(pair + 1 + j) * 2 + rank] = 0u;
+            } else {
+                uint32_t packed[BN / 2];
+#pragma unroll
+                for (int c = 0; c < BN / 16; ++c) {
+                    uint32_t v[16];
+                    acc_chunk<BN>(t1, t2, c, branch, keep, v);
+                    float f[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]);
+                    if (!kBwd && p.col_scale != nullptr) col_scale_chunk(p, n0 + c * 16, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) packed[c * 8 + e] = pack_bf16x2(f[2 * e], f[2 * e + 1]);
                 }
-                sb ^= 1;
+                // all of this tile's TMEM reads are done: hand the accumulator back
+                tc_fence_before();
+                mbar_arrive_cluster(peer_addr(smem_u32(&acc_empty[b]), 0));
+#pragma unroll
+                for (int blk = 0; blk < BN / 64; ++blk) store_block(p.mapOut, staging, sb, issuer, er, packed + blk * 32, n0 + blk * 64, m0);
             }
             ++use;
         }
@@ -429,12 +554,12 @@ cudaError_t gemm2_configure() {
                                 static_cast<int>(smem_bytes<true, 128>()));
 }
 
-cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStream_t stream) {
-    const int n_mp = static_cast<int>((p.M + 255) / 256);
-    const int n_np = static_cast<int>((p.N + bn - 1) / bn);
-    int pairs = n_mp * n_np;
-    if (pairs > sms / 2) pairs = sms / 2;
-    if (pairs < 1) pairs = 1;
+GemmSched plan_gemm2(const GemmParams& p, bool bwd, int bn, int sms, bool allow_split) {
+    const bool single_acc = bwd ? !Cfg<true, 256>::kDouble && bn == 256 : false;
+    return gemm_schedule(p.M, p.N, bn, (p.nkb + kKB - 1) / kKB, sms / 2, allow_split, single_acc);
+}
+
+cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int pairs, cudaStream_t stream) {
     const dim3 grid(2 * pairs);
     if (!bwd) return launch_pdl(gemm2_kernel<false, 256>, grid, dim3(kThreads), smem_bytes<false, 256>(), stream, p);
     if (bn == 128) return launch_pdl(gemm2_kernel<true, 128>, grid, dim3(kThreads), smem_bytes<true, 128>(), stream, p);

@@ -65,7 +65,10 @@ cudaError_t launch_finalize_s(const DownParams& p, int sms, cudaStream_t stream)
 // buffers); backward 256 x kBwdPairBN (acc1 + acc2 fill TMEM: one buffer).
 constexpr int kBwdPairBN = 256;
 cudaError_t gemm2_configure();
-cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int sms, cudaStream_t stream);
+// Grid and split tiles for a call (p.M, p.N, p.nkb set); `allow_split` false when the workspace has no
+// partial slots.  The launch takes p.sk_tiles as set from it and the schedule's pair count.
+GemmSched plan_gemm2(const GemmParams& p, bool bwd, int bn, int sms, bool allow_split);
+cudaError_t launch_gemm2(const GemmParams& p, bool bwd, int bn, int pairs, cudaStream_t stream);
 
 size_t dsdb_smem_bytes(const DsDbParams& p);
 cudaError_t dsdb_configure();

@@ -6,6 +6,7 @@
 // adapter id and that adapter's rank, scale and dropout rate).
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 
@@ -114,7 +115,96 @@ struct GemmParams {
     int32_t early_loads;               // 1: the producer may load the first tile's main-loop stages before waiting on
                                        // the previous kernel (no kernel of this call writes the main-loop operands, and
                                        // an earlier kernel of the call has already waited on the caller's work)
+    int32_t sk_tiles;                  // stream-K: tiles [0, sk_tiles) are cut into runs of K stages spread evenly over
+                                       // the pairs (0: every tile goes whole to one pair)
+    float* sk_part;                    // per pair and CTA rank: the fp32 partial of the pair's first run when that run
+                                       // is not the start of its tile (kSkSlotFloats each)
+    uint32_t* sk_flag;                 // per pair and CTA rank: 1 once that partial is stored; reset by its reader
 };
+
+// Stream-K split tiles of the pair GEMM.  A pair's runs cover the contiguous units (tile, K stage)
+// [U c / P, U (c+1) / P) of the first sk_tiles tiles, U = sk_tiles * stages, then whole tiles.  Only a pair's
+// first run can start inside a tile, so one partial slot per pair and CTA suffices.  The run that starts a
+// split tile adds the other runs' partials to its own accumulator in pair order and stores the tile.
+constexpr int kSkSlotFloats = 128 * 256;   // 128 rows x up to 256 columns
+constexpr int kSkMaxParts = 2;             // other runs per split tile (the schedule keeps U / P >= stages / 2)
+constexpr int kSkMinStages = 32;           // below this many K stages no tile is split
+
+struct GemmSched {
+    int32_t pairs;      // CTA pairs in the grid
+    int32_t sk_tiles;   // tiles split by K (GemmParams::sk_tiles)
+};
+
+// Tiles T of 256 rows x bn columns, `stages` K stages each, `max_pairs` pairs that fit the device.  Whole
+// tiles go to pairs in turn (min(T, max_pairs) pairs).  Splitting costs a partial store and read per split
+// tile (a closing run's epilogue takes about as long as 26 stages of main loop), and the split runs start at
+// staggered K offsets, which shares fewer operand lines in L2.  So tiles are split only where a last wave
+// leaves most pairs idle and tiles have at least kSkMinStages stages (on GB300 splitting lost at 16):
+//  - 2T <= max_pairs: every tile split in two, over 2T pairs;
+//  - W = T / max_pairs full waves and R = T mod max_pairs > 0 tiles left: the first R + max_pairs tiles are
+//    split (between one and two tiles of stages a pair) when R <= max_pairs / 4; or when R <= max_pairs / 2,
+//    the closing runs are followed by whole tiles whose main loops hide them (W >= 2, two accumulator
+//    sets) and the tiles are at most 64 stages deep (measured: a gain at 64 stages, none at 128).
+// The split runs come first in every pair's order, so a split tile's closing run (which reads the other
+// runs' partials) is followed by whole tiles.
+inline GemmSched gemm_schedule(int64_t M, int64_t N, int bn, int stages, int max_pairs, bool allow_split,
+                               bool single_acc) {
+    const int64_t T = ((M + 255) / 256) * ((N + bn - 1) / bn);
+    if (max_pairs < 1) max_pairs = 1;
+    GemmSched s{static_cast<int32_t>(std::max<int64_t>(1, std::min<int64_t>(T, max_pairs))), 0};
+    if (!allow_split || T == 0 || stages < kSkMinStages) return s;
+    if (2 * T <= max_pairs) {
+        s.pairs = static_cast<int32_t>(2 * T);
+        s.sk_tiles = static_cast<int32_t>(T);
+        return s;
+    }
+    if (T < max_pairs) return s;
+    const int64_t W = T / max_pairs, R = T % max_pairs;
+    const bool hidden = W >= 2 && !single_acc && stages <= 64;
+    if (R != 0 && (hidden ? 2 * R <= max_pairs : 4 * R <= max_pairs)) s.sk_tiles = static_cast<int32_t>(R + max_pairs);
+    return s;
+}
+
+// One run of a pair's work: main-loop stages [kb0, kb1) of a tile.  A run that ends at the last stage also
+// takes the tile's rank-r tail; a run that is not the whole tile is part of a split tile.
+struct Run {
+    int tile, kb0, kb1;
+};
+
+__host__ __device__ __forceinline__ int64_t sk_unit_begin(int pair, int64_t U, int npairs) {
+    return U * pair / npairs;
+}
+
+// A pair's runs in order: its units [U c / P, U (c+1) / P) of the first sk_tiles tiles (one run per tile
+// touched), then whole tiles sk_tiles + c, + P, ...
+struct RunWalk {
+    int64_t u, u_end;
+    int tile, total, step, nk;
+
+    __host__ __device__ __forceinline__ bool next(Run& r) {
+        if (u < u_end) {
+            const int t = static_cast<int>(u / nk);
+            const int kb0 = static_cast<int>(u - static_cast<int64_t>(t) * nk);
+            const int64_t left = u_end - u;
+            const int kb1 = left < nk - kb0 ? kb0 + static_cast<int>(left) : nk;
+            r = Run{t, kb0, kb1};
+            u += kb1 - kb0;
+            return true;
+        }
+        if (tile < total) {
+            r = Run{tile, 0, nk};
+            tile += step;
+            return true;
+        }
+        return false;
+    }
+};
+
+__host__ __device__ __forceinline__ RunWalk run_walk(int sk_tiles, int pair, int npairs, int nk, int total) {
+    const int64_t U = static_cast<int64_t>(sk_tiles) * nk;
+    return RunWalk{sk_unit_begin(pair, U, npairs), sk_unit_begin(pair + 1, U, npairs), sk_tiles + pair, total,
+                   npairs, nk};
+}
 
 // dS / dB from one read of dY: per (active tile, 128-wide n-block) unit,
 //   acc_dS[tile]  += dY_tile B_a^T

@@ -21,6 +21,7 @@ EXPORTED = ["lora_workspace_size", "lora_set_deterministic", "lora_get_determini
             "dora_workspace_size", "dora_weight_norm2", "dora_fwd", "dora_bwd",
             "lora_fwd_static_scratch", "lora_tile_table",
             "lora_keep_threshold", "lora_pack_greedy", "lora_device_status", "lora_set_wait_limit_ns", "lora_debug_stuck_wait",
+            "lora_debug_gemm_runs",
             "lora_status_string", "lora_timing_begin", "lora_timing_end", "lora_kernel_name",
             "lora_last_error_string"]
 
@@ -85,6 +86,9 @@ def lib() -> ctypes.CDLL:
             "lora_device_status": (i32, [vp, vp, ctypes.POINTER(ctypes.c_int32)]),
             "lora_set_wait_limit_ns": (None, [u64]),
             "lora_debug_stuck_wait": (i32, [vp, sz, vp]),
+            "lora_debug_gemm_runs": (i32, [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), i64,
+                                           ctypes.POINTER(ctypes.c_int64)]),
             "lora_status_string": (ctypes.c_char_p, [i32]),
             "lora_last_error_string": (ctypes.c_char_p, []),
             "lora_timing_begin": (i32, []),
@@ -164,6 +168,21 @@ def pack_microbatches(lengths, adapters, capacity: int):
         b["valid"].append(int(lengths[i]))
         b["rows"] = row[i] + rows
     return out
+
+
+def gemm_runs(M: int, N: int, bn: int, stages: int, max_pairs: int, allow_split: bool = True,
+              single_acc: bool = False):
+    """The pair GEMM's schedule from the library (host only).
+
+    Returns (pairs, split_tiles, runs), runs a list of (pair, tile, first stage, end stage) in the order
+    each pair works through them."""
+    pairs, split, n = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int64(0)
+    args = (M, N, bn, stages, max_pairs, int(allow_split), int(single_acc), ctypes.byref(pairs), ctypes.byref(split))
+    check("lora_debug_gemm_runs", lib().lora_debug_gemm_runs(*args, None, 0, ctypes.byref(n)))
+    buf = (ctypes.c_int32 * (4 * max(1, n.value)))()
+    check("lora_debug_gemm_runs", lib().lora_debug_gemm_runs(*args, buf, n.value, ctypes.byref(n)))
+    runs = [tuple(buf[4 * i:4 * i + 4]) for i in range(n.value)]
+    return pairs.value, split.value, runs
 
 
 KERNEL_KINDS = 13

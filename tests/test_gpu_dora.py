@@ -52,6 +52,7 @@ def check(raw, mag, out, alpha, p, seed):
     (200, 264, 392, 8, 1.5, 0.2, 71),          # ragged m, k, n; rank 8 (padded 16)
     (384, 512, 768, 64, 2.0, 0.05, 72),
     (130, 1024, 256, 128, 0.5, 0.0, 73),      # rank 128, no dropout
+    (256, 2048, 512, 16, 2.0, 0.1, 74),       # forward tiles split by K: the column scale after the partials' sum
 ])
 def test_dora_matches_oracle(m, k, n, r, alpha, p, seed):
     raw, mag, out = run(m, k, n, r, alpha, p, seed)

@@ -66,12 +66,18 @@ def test_single_shapes(m, k, n, r, alpha, p, seed):
     check_single_full(raw, out, alpha, p, seed)
 
 
-# Shapes whose GEMMs leave CTA pairs idle: fewer tiles than pairs, and three full waves plus a partial one,
-# at larger k and n than the other cases (the square 4096 sweep's small-m points), with rank-r tails.
+# Shapes whose GEMMs leave CTA pairs idle: fewer tiles than pairs, and full waves plus a partial one, at
+# larger k and n than the other cases (the square 4096 sweep's small-m points), with rank-r tails.  Where
+# the last wave leaves most of the 76 pairs idle the GEMMs split tiles by K (stream-K runs whose partial
+# sums the run holding stage 0 adds): those cases check the split path, the branch tail in a run that does
+# not start its tile, and the keep bits it hands to the dA pass.
 @pytest.mark.parametrize("m,k,n,r,alpha,p,seed", [
-    (1024, 4096, 4096, 16, 2.0, 0.1, 61),     # 64 tiles in each GEMM
-    (768, 2048, 3072, 64, 1.0, 0.2, 62),      # 36 forward tiles, 24 backward tiles
-    (4096, 4096, 4096, 32, 2.0, 0.1, 63),     # 256 tiles: three full waves, the fourth 28 tiles
+    (1024, 4096, 4096, 16, 2.0, 0.1, 61),     # 64 tiles in each GEMM (whole tiles)
+    (768, 2048, 3072, 64, 1.0, 0.2, 62),      # 36 forward tiles, 24 backward tiles: each split in two
+    (4096, 4096, 4096, 32, 2.0, 0.1, 63),     # 256 tiles: three full waves + 28; the forward splits 104
+    (1280, 4096, 2048, 16, 2.0, 0.1, 64),     # backward 80 tiles (one wave + 4): all split; keep bits to dA
+    (2560, 2048, 4096, 32, 1.0, 0.1, 65),     # forward 160 tiles (two waves + 8): the first 84 split;
+                                              # backward 80 tiles, all split
 ])
 def test_partial_wave_shapes(m, k, n, r, alpha, p, seed):
     raw, out = run_single(m, k, n, r, alpha, p, seed)

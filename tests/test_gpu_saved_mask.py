@@ -29,6 +29,7 @@ SAME = 4e-3
     (200, 288, 392, 32, 1.5, 0.2, 82),       # k % 32 == 0 only; ragged m
     (130, 264, 256, 8, 1.0, 0.3, 83),        # k % 8 only: both regenerate
     (256, 4096, 320, 64, 2.0, 0.5, 84),      # many k blocks
+    (384, 1024, 2048, 16, 2.0, 0.1, 85),     # backward tiles split by K: the run holding the tail reads the bits
 ])
 def test_single_backward_with_saved_bits(m, k, n, r, alpha, p, seed):
     raw = synth.layer_inputs(seed, m, k, n, r)
