@@ -116,7 +116,7 @@ typedef struct {
  * needs a larger workspace, sized for the current device.
  *
  * The last region of this size holds the partial sums of GEMM output tiles
- * whose K loop is split over several CTA pairs (up to 80 pairs x 256 KB, 20
+ * whose K loop is split over several CTA pairs (up to 80 pairs x 256 KB, 21
  * MB; less when the GEMMs have few tiles).  A call whose workspace ends before
  * that region still runs, with every tile computed whole by one pair: the GEMMs
  * then leave more CTA pairs idle when their last wave of tiles is nearly empty.
