@@ -54,6 +54,7 @@ def assert_bit_identical(a, b, names):
     (2048, 2048, 4096, 64, 0.1),     # strip-order rank: dS pass in tile order, dB pass on one-block strips
     (300, 1024, 512, 128, 0.05),     # largest rank, ragged rows
     (512, 4096, 2048, 32, 0.1),      # both GEMMs split tiles by K: partials added in pair order
+    (512, 1024, 4096, 16, 0.1),      # eight backward tiles, each split in two by K
 ])
 def test_single_adapter_bit_identical_and_correct(deterministic, m, k, n, r, p):
     alpha, seed = 2.0, 41

@@ -78,6 +78,8 @@ def test_single_shapes(m, k, n, r, alpha, p, seed):
     (1280, 4096, 2048, 16, 2.0, 0.1, 64),     # backward 80 tiles (one wave + 4): all split; keep bits to dA
     (2560, 2048, 4096, 32, 1.0, 0.1, 65),     # forward 160 tiles (two waves + 8): the first 84 split;
                                               # backward 80 tiles, all split
+    (640, 2048, 8192, 64, 2.0, 0.2, 66),      # rank 64, 128 K stages in the backward
+    (384, 1032, 3072, 8, 1.0, 0.1, 67),       # rank 8; k % 128 != 0 (dA regenerates the mask), a ragged column tile
 ])
 def test_partial_wave_shapes(m, k, n, r, alpha, p, seed):
     raw, out = run_single(m, k, n, r, alpha, p, seed)
