@@ -595,6 +595,11 @@ lora_status run_bwd(const Call& c, const uint16_t* dY, const uint16_t* X, const 
         p.parts = kPartDs | kPartDb;
         const int64_t ctas = static_cast<int64_t>(two_per_sm ? 2 : 1) * c.sms;
         if (!c.det) {
+            // up to padded rank 64 four threads issue the strip order's MMAs: two dS accumulators per buffer
+            // leave TMEM for four n-blocks a strip (k_dsdb.cu, dsdb_strip4_kernel).  Measured on the 70B up-proj at
+            // rank 64: 257 -> 213 us for the pass, 9.245 -> 9.155 ms for the step.
+            if (p.strip > 0 && strip_four_issuers(static_cast<int>(rpm), p.parts))
+                p.strip = std::max(1, std::min<int>(p.nnb, (two_per_sm ? 256 : 512) / static_cast<int>(rpm) - 4));
             const int grid = static_cast<int>(std::min<int64_t>(p.units, ctas));
             LORA_CUDA(timed(kDsDb, c.stream, [&] { return launch_dsdb(p, grid, c.stream); }));
             LORA_CUDA(timed(kFinalize, c.stream, [&] { return launch_finalize_bwd1(p, kPartDs | kPartDb, c.sms, c.stream); }));

@@ -26,7 +26,8 @@
 //    (dS), plus one flush of the strip's dB^T accumulators per segment: at
 //    rank 64 a sixth of the bytes of the tile order.
 // In both orders two threads issue the MMAs of a stage (dS and dB^T): a small
-// MMA costs its issuing thread a fixed time whatever its size.  Where two
+// MMA costs its issuing thread a fixed time whatever its size.  The strip
+// order up to padded rank 64 uses four (dsdb_strip4_kernel below).  Where two
 // stages fit in half the shared memory (padded rank <= 32) two CTAs share each
 // SM with two-stage rings; otherwise one CTA per SM holds the deepest ring.
 // Either way finalize_bwd1 then scales and rounds the sums (dSq =
@@ -40,6 +41,7 @@ namespace lora {
 namespace {
 
 constexpr int kThreads = 224;   // warp 0 TMA, warp 1 dS MMA issuer, warps 2-5 epilogue, warp 6 dB MMA issuer
+constexpr int kThreads4 = 288;
 constexpr uint32_t kDyBytes = 2u * 128u * 128u;   // 128 tokens x 128 n
 
 // Walks units from u0 on in strip order (strip s of width w, active tile slot,
@@ -569,6 +571,290 @@ __global__ void __launch_bounds__(kThreads, 2) dsdb_strip_kernel(const __grid_co
     }
 }
 
+// Strip order with four MMA-issuing threads (padded rank <= 64, even strip width).  One thread issues a
+// small tcgen05 MMA about every 250-300 cycles however many accumulators it feeds, and independent issuing
+// warps add up (measured on GB300 with M128 N64 K16 MMAs: 1, 2, 4 and 8 issuers gave one MMA per 318, 155,
+// 79 and 49 cycles per SM).  So the dS MMAs of a unit are shared by two threads, each into its own
+// accumulator (the 64-deep halves of the unit's n-block; the epilogue adds the two), and the dB^T MMAs of a
+// unit go to one of two threads by the parity of its n-block within the strip, each n-block keeping one
+// accumulator.  TMEM: two dS buffers per dS thread, then one dB^T accumulator per n-block of a strip.
+__global__ void __launch_bounds__(kThreads4, 2) dsdb_strip4_kernel(const __grid_constant__ DsDbParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    const int S = p.stages;
+    const int J = p.strip;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * p.stage_bytes);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + S;             // all four issuers: both dS threads commit, the dB^T thread of the
+                                            // unit's parity commits and the other one arrives
+    uint64_t* accS_full = bars + 2 * S;     // [2]: both dS threads commit
+    uint64_t* accS_empty = accS_full + 2;   // [2]
+    uint64_t* accB_full = accS_empty + 2;   // [2]: per n-block parity
+    uint64_t* accB_empty = accB_full + 2;   // [2]: per n-block parity
+    uint64_t* drain = accB_empty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rpad_max = p.rt.rpad_max;
+    uint32_t tmem_cols = 32;
+    while (tmem_cols < static_cast<uint32_t>((4 + J) * rpad_max)) tmem_cols <<= 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accS_full[b], 2);
+            mbar_init(&accS_empty[b], 128);
+            mbar_init(&accB_full[b], 1);
+            mbar_init(&accB_empty[b], 128);
+        }
+        mbar_init(drain, 4);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.mapDY);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_wait();
+    pdl_trigger();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t rp = static_cast<uint32_t>(rpad_max);
+    const uint32_t tB = tmem + 4u * rp;   // dB^T: one per n-block of a strip
+    const WaitCtx w{&abort_flag, p.ctl.status, p.ctl.wait_ns, kKDsDb << 8};
+
+    const int64_t U = p.units;
+    const int64_t u0 = U * blockIdx.x / gridDim.x;
+    const int64_t u1 = U * (blockIdx.x + 1) / gridDim.x;
+    const uint32_t bbox = rp * 128u;   // spacing of the two B boxes
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            StripIter it(u0, J, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int nb = it.nb();
+                const int tile = it.tile;
+                const int a = it.a;
+                const int rpad = p.rt.ad[a].rpad;
+                if (!mbar_wait(&empty[s], ph ^ 1u, w, 1)) { ok = false; break; }
+                uint8_t* st = smem + s * p.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], kDyBytes + 2u * 128u * rpad + 256u * rpad);
+                tma_load_2d(st, &p.mapDY, &full[s], nb * 128, tile * kTileM);
+                tma_load_2d(st + 16384, &p.mapDY, &full[s], nb * 128 + 64, tile * kTileM);
+                tma_load_2d(st + p.off_b, &p.mapB[a], &full[s], nb * 128, 0);
+                tma_load_2d(st + p.off_b + bbox, &p.mapB[a], &full[s], nb * 128 + 64, 0);
+                tma_load_2d(st + p.off_s, &p.mapS[a], &full[s], 0, tile * kTileM);
+                if (rpad > 64) tma_load_2d(st + p.off_s + 16384, &p.mapS[a], &full[s], 64, tile * kTileM);
+                ++issued;
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            if (!ok) {
+                const int64_t back = issued < S ? issued : S;
+                for (int64_t i = issued - back; i < issued; ++i)
+                    mbar_wait_drain(&full[i % S], static_cast<uint32_t>((i / S) & 1), p.ctl.wait_ns);
+            }
+        }
+    } else if (warp == 1 || warp == 7) {
+        // dS (+)= dY_tile * B_a^T over one 64-deep half of the unit's n-block: warp 1 the first, warp 7 the second
+        if (lane == 0) {
+            const uint32_t h = warp == 1 ? 0u : 1u;
+            const uint32_t tS = tmem + 2u * h * rp;
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t visits = 0;
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t ds_a0 = make_smem_desc(sbase, 16, 1024, kSw128) + h * 1024u;                      // dY, K-major
+            const uint64_t ds_b0 = make_smem_desc(sbase + p.off_b, 16, 1024, kSw128) + h * (bbox >> 4);      // B_a, K-major
+            int cur_rpad = -1;
+            uint32_t idesc_s = 0;
+            StripIter it(u0, J, p.nnb, p.rt);
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const int rpad = p.rt.ad[it.a].rpad;
+                if (rpad != cur_rpad) {
+                    cur_rpad = rpad;
+                    idesc_s = make_idesc_bf16(128, rpad, false, false);
+                }
+                const bool visit_first = (u == u0) || it.j == 0;
+                const bool visit_last = (u == u1 - 1) || it.j == it.w - 1;
+                const uint32_t bs = visits & 1u;
+                if (visit_first) {
+                    if (!mbar_wait(&accS_empty[bs], ((visits >> 1) & 1u) ^ 1u, w, 3)) break;
+                    tc_fence_after();
+                }
+                if (!mbar_wait(&full[s], ph, w, 4)) break;
+                tc_fence_after();
+                const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
+                const uint32_t dS_acc = tS + bs * rp;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_bf16(dS_acc, ds_a0 + so + kk * 2u, ds_b0 + so + kk * 2u, idesc_s, (visit_first && kk == 0) ? 0u : 1u);
+                umma_commit(&empty[s]);
+                if (visit_last) {
+                    umma_commit(&accS_full[bs]);
+                    ++visits;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else if (warp == 6 || warp == 8) {
+        // dB^T[n-block] (+)= dY_tile^T * S'_tile for the units whose n-block has this thread's parity
+        if (lane == 0) {
+            const int par = warp == 6 ? 0 : 1;
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t segs = 0, used = 0;
+            bool had = false;   // this thread has MMAs in the current segment
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t db_a0 = make_smem_desc(sbase, 16384, 1024, kSw128);   // dY^T, MN-major
+            int cur_rpad = -1;
+            uint32_t idesc_b = 0, rb = 0;
+            uint64_t db_b0 = 0;
+            StripIter it(u0, J, p.nnb, p.rt);
+            bool ok = true;
+            for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+                const bool seg_last = (u == u1 - 1) || it.segment_ends(p.rt);
+                // Every stage's phase is waited on, the other parity's too: a parity wait tells two phases apart
+                // only if the waiter sees each one, and a thread that skipped stages could take an older
+                // completion of this stage's barrier for the current one.
+                if ((it.j & 1) != par) {
+                    if (!mbar_wait(&full[s], ph, w, 4)) { ok = false; break; }
+                    mbar_arrive(&empty[s]);
+                } else {
+                    const int rpad = p.rt.ad[it.a].rpad;
+                    if (rpad != cur_rpad) {
+                        cur_rpad = rpad;
+                        idesc_b = make_idesc_bf16(128, rpad, true, true);
+                        rb = rank_row_bytes(rpad);
+                        db_b0 = make_smem_desc(sbase + p.off_s, 16384, 8u * rb, rank_swizzle(rpad));   // S', MN-major
+                    }
+                    if (!had) {
+                        // the previous segment's dB^T accumulators of this parity have been flushed
+                        if (!mbar_wait(&accB_empty[par], (segs & 1u) ^ 1u, w, 2)) { ok = false; break; }
+                        tc_fence_after();
+                        used = 0;
+                        had = true;
+                    }
+                    if (!mbar_wait(&full[s], ph, w, 4)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t so = (static_cast<uint32_t>(s) * p.stage_bytes) >> 4;
+                    const uint32_t dB_acc = tB + static_cast<uint32_t>(it.j) * rp;
+                    const bool fresh = ((used >> it.j) & 1u) == 0u;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)
+                        umma_bf16(dB_acc, db_a0 + so + ks * 128u, db_b0 + so + static_cast<uint64_t>(ks) * rb, idesc_b,
+                                  (fresh && ks == 0) ? 0u : 1u);
+                    used |= 1u << it.j;
+                    umma_commit(&empty[s]);
+                }
+                if (seg_last && had) {
+                    umma_commit(&accB_full[par]);
+                    ++segs;
+                    had = false;
+                }
+                if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            (void)ok;
+            umma_commit(drain);
+            mbar_wait_drain(drain, 0, p.ctl.wait_ns);
+        }
+    } else if (warp >= 2 && warp <= 5) {
+        const int quad = warp & 3;
+        const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t visits = 0, used = 0, present = 0;
+        uint32_t segs[2] = {0u, 0u};
+        StripIter it(u0, J, p.nnb, p.rt);
+        for (int64_t u = u0; u < u1; ++u, it.next(p.rt)) {
+            const AdapterDev ad = p.rt.ad[it.a];
+            const bool visit_last = (u == u1 - 1) || it.j == it.w - 1;
+            const bool seg_last = (u == u1 - 1) || it.segment_ends(p.rt);
+            used |= 1u << it.j;
+            present |= 1u << (it.j & 1);
+            if (visit_last) {
+                const uint32_t bs = visits & 1u;
+                const bool ok = mbar_wait(&accS_full[bs], (visits >> 1) & 1u, w, 5);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                const int64_t row = static_cast<int64_t>(it.tile) * kTileM + quad * 32 + lane;
+                float* dst = p.dS_acc + row * p.ld;
+                const uint32_t t0 = tmem + lane_off + bs * rp;             // first half's accumulator
+                const uint32_t t1 = tmem + lane_off + (2u + bs) * rp;      // second half's
+                for (int c0 = 0; (p.parts & kPartDs) && c0 < ad.rpad; c0 += 16) {
+                    uint32_t v[16], x[16];
+                    tmem_ld16(t0 + c0, v);
+                    tmem_ld16(t1 + c0, x);
+                    tmem_ld_wait();
+                    if (row < p.m) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (c0 + q < ad.rank)
+                                red_add_v4(dst + c0 + q, __uint_as_float(v[q]) + __uint_as_float(x[q]),
+                                           __uint_as_float(v[q + 1]) + __uint_as_float(x[q + 1]),
+                                           __uint_as_float(v[q + 2]) + __uint_as_float(x[q + 2]),
+                                           __uint_as_float(v[q + 3]) + __uint_as_float(x[q + 3]));
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&accS_empty[bs]);
+                ++visits;
+            }
+            if (seg_last) {
+                bool ok = true;
+                for (int par = 0; par < 2; ++par)
+                    if ((present >> par) & 1u) ok = ok && mbar_wait(&accB_full[par], segs[par] & 1u, w, 6);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after();
+                for (int jj = 0; (p.parts & kPartDb) && jj < it.w; ++jj) {
+                    if (!((used >> jj) & 1u)) continue;
+                    const int64_t nidx = static_cast<int64_t>(it.s * J + jj) * 128 + quad * 32 + lane;
+                    float* dst = p.acc_base + ad.dB_off + nidx * ad.rpad;
+                    const uint32_t taddr = tB + lane_off + static_cast<uint32_t>(jj) * rp;
+                    for (int c0 = 0; c0 < ad.rpad; c0 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(taddr + c0, v);
+                        tmem_ld_wait();
+                        if (nidx < p.n) {
+#pragma unroll
+                            for (int q = 0; q < 16; q += 4)
+                                if (c0 + q < ad.rank)
+                                    red_add_v4(dst + c0 + q, __uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                                               __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+                        }
+                    }
+                }
+                tc_fence_before();
+                for (int par = 0; par < 2; ++par)
+                    if ((present >> par) & 1u) {
+                        mbar_arrive(&accB_empty[par]);
+                        ++segs[par];
+                    }
+                used = 0;
+                present = 0;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
 // dSq[t, c] = bf16(alpha_a / (1 - p_a) * dS_acc[t, c]) for c < r_a, else 0, on
 // rows of active tiles (parts & kPartDs); dB_a[c, j] = bf16(dB^T_acc_a[j, c])
 // (parts & kPartDb).  Every accumulator read is cleared.
@@ -666,15 +952,19 @@ __global__ void __launch_bounds__(256, 4) finalize_bwd1_kernel(float* __restrict
 
 }  // namespace
 
-size_t dsdb_smem_bytes(const DsDbParams& p) { return 1024 + p.stages * p.stage_bytes + (2 * p.stages + 7) * 8 + 16; }
+size_t dsdb_smem_bytes(const DsDbParams& p) { return 1024 + p.stages * p.stage_bytes + (2 * p.stages + 9) * 8 + 16; }
 
 cudaError_t dsdb_configure() {
-    const cudaError_t e = cudaFuncSetAttribute(dsdb_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    cudaError_t e = cudaFuncSetAttribute(dsdb_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dsdb_strip4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(dsdb_strip_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
 }
 
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream) {
+    if (p.strip > 0 && strip_four_issuers(p.rt.rpad_max, p.parts))
+        return launch_pdl(dsdb_strip4_kernel, dim3(grid), dim3(kThreads4), dsdb_smem_bytes(p), stream, p);
     if (p.strip > 0) return launch_pdl(dsdb_strip_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
     return launch_pdl(dsdb_tile_kernel, dim3(grid), dim3(kThreads), dsdb_smem_bytes(p), stream, p);
 }

@@ -75,6 +75,10 @@ cudaError_t dsdb_configure();
 cudaError_t launch_dsdb(const DsDbParams& p, int grid, cudaStream_t stream);
 // finalize_bwd1 parts: dSq from dS (the dX GEMM and dA need it) and dB from dB^T (an output only).
 constexpr int kPartDs = 1, kPartDb = 2;
+// The strip order issues its MMAs from four threads up to padded rank 64 when it flushes both products: two
+// dS accumulators per buffer leave TMEM for four n-blocks a strip (columns / rpad - 4) instead of six
+// (columns / rpad - 2).  The host sizes the strip and launch_dsdb picks the kernel by the same test.
+inline bool strip_four_issuers(int rpad_max, int parts) { return rpad_max <= 64 && parts == (kPartDs | kPartDb); }
 cudaError_t launch_finalize_bwd1(const DsDbParams& p, int parts, int sms, cudaStream_t stream, bool pdl = true);
 
 size_t da_smem_bytes(const DaParams& p);
